@@ -1,0 +1,582 @@
+// C ABI of the compression-stage library: argument checks, workspace layout, launch
+// configuration and launches on the caller's stream. See include/ob.h for the contract.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/ob.h"
+#include "ob_internal.h"
+
+using namespace ob;
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+constexpr size_t kAlignWs = 256;
+constexpr int kWarpsPerBlock = kBlock / 32;
+
+size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    size_t wbits, sbits, mask, s_prev, s_next, t_prev, t_next, wpart, spart, wcnt, scnt, total;
+};
+
+struct Rec {
+    int kernel;
+    cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct ob_ctx {
+    int64_t n = 0, C = 0, nchunks = 0;
+    int W = 0;
+    float b1 = 0, b2 = 0, eps = 0, lr = 0, wd = 0;
+    int bias_correction = 0;
+    int64_t step = 0;
+    int device = -1;
+    int sms = 152;
+    Part pt{};
+    Layout lay{};
+    bool has_mask = false;
+    int64_t launches = 0;
+    bool profiling = false;
+    std::vector<Rec> recs;
+    std::vector<cudaEvent_t> spare;
+    double prof_ms[OB_K_COUNT] = {};
+    int64_t prof_n[OB_K_COUNT] = {};
+};
+
+namespace {
+
+int cuda_fail(cudaError_t e)
+{
+    g_last_cuda = (int)e;
+    return OB_ECUDA;
+}
+
+int check_ptr(const void* p, size_t align)
+{
+    if (!p) return OB_EINVAL;
+    if (reinterpret_cast<uintptr_t>(p) % align) return OB_EALIGN;
+    return OB_OK;
+}
+
+// The device the context was created on must be current.
+int check_device(const ob_ctx* c)
+{
+    int d = -1;
+    const cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return d == c->device ? OB_OK : OB_EINVAL;
+}
+
+cudaEvent_t take_event(ob_ctx* c)
+{
+    if (!c->spare.empty()) {
+        cudaEvent_t e = c->spare.back();
+        c->spare.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Launch wrapper: counts launches and, when profiling, brackets them with events.
+template <typename F>
+int launch(ob_ctx* c, int kernel, cudaStream_t s, F&& f)
+{
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (c->profiling) {
+        a = take_event(c);
+        b = take_event(c);
+        if (a && b) cudaEventRecord(a, s);
+    }
+    const cudaError_t e = f();
+    if (e != cudaSuccess) return cuda_fail(e);
+    ++c->launches;
+    if (a && b) {
+        cudaEventRecord(b, s);
+        c->recs.push_back(Rec{kernel, a, b});
+    }
+    return OB_OK;
+}
+
+int stream_grid(const ob_ctx* c) { return c->sms * 8; }
+
+// Worker/server grids: all resident blocks, rounded down to a power of two per SM so
+// that P (a multiple of the SM count times a power of two) splits evenly over warps.
+int pow2_floor(int v)
+{
+    int p = 1;
+    while (p * 2 <= v) p *= 2;
+    return v < 1 ? 1 : p;
+}
+
+Layout make_layout(int64_t n, int W, int64_t nch, int64_t P, int64_t J)
+{
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = up(off + bytes, kAlignWs);
+        return at;
+    };
+    L.wbits = take((size_t)W * (n / 8));
+    L.sbits = take((size_t)n / 8);
+    L.mask = take((size_t)n / 8);
+    L.s_prev = take((size_t)W * nch * 4);
+    L.s_next = take((size_t)W * nch * 4);
+    L.t_prev = take((size_t)nch * 4);
+    L.t_next = take((size_t)nch * 4);
+    L.wpart = take((size_t)W * P * J * 8);
+    L.spart = take((size_t)P * J * 8);
+    L.wcnt = take((size_t)nch * 4);
+    L.scnt = take((size_t)nch * 4);
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off)
+{
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int check_grads(const ob_ctx* c, const void* g, int dtype)
+{
+    if (dtype != OB_F32 && dtype != OB_F16 && dtype != OB_BF16) return OB_EINVAL;
+    return check_ptr(g, 16);
+}
+
+int grad_bytes(int dtype) { return dtype == OB_F32 ? 4 : 2; }
+
+bool finite(float v) { return std::isfinite(v); }
+
+}  // namespace
+
+extern "C" {
+
+int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, float lr,
+            ob_ctx** out)
+{
+    if (!out) return OB_EINVAL;
+    if (W < 1 || W > 16 || n <= 0 || chunk <= 0) return OB_EINVAL;
+    if (n % ((int64_t)W * 256) != 0) return OB_EINVAL;
+    if (chunk % 256 != 0 || (n / W) % chunk != 0) return OB_EINVAL;
+    if (!finite(b1) || !finite(b2) || !finite(eps) || !finite(lr)) return OB_EINVAL;
+    if (b1 < 0.0f || b1 >= 1.0f || b2 < 0.0f || b2 >= 1.0f || eps < 0.0f) return OB_EINVAL;
+
+    ob_ctx* c = new (std::nothrow) ob_ctx();
+    if (!c) return OB_EINVAL;
+    c->n = n;
+    c->W = W;
+    c->C = chunk;
+    c->nchunks = n / chunk;
+    c->b1 = b1;
+    c->b2 = b2;
+    c->eps = eps;
+    c->lr = lr;
+
+    // Device facts; on a machine without a GPU the context can still be created (for
+    // argument checks), sized for a 152-SM part, and every launch will fail.
+    int dev = -1, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+        c->device = dev;
+        c->sms = sms;
+    } else {
+        cudaGetLastError();
+        c->device = -1;
+        c->sms = 152;
+    }
+    int occ = 0;
+    if (c->device >= 0)
+        for (int dt = 0; dt < 3; ++dt) occ = occ > occupancy_worker(W, dt) ? occ : occupancy_worker(W, dt);
+    if (occ <= 0) occ = 2;
+    occ = pow2_floor(occ);
+
+    Part pt{};
+    pt.NG = n / 256;
+    pt.CG = chunk / 256;
+    pt.nchunks = c->nchunks;
+    const int64_t want = (int64_t)c->sms * occ * kWarpsPerBlock;
+    pt.P = want < pt.NG ? want : pt.NG;
+    int64_t J = 1;
+    for (int64_t q = 0; q < pt.P; ++q) {
+        const int64_t g0 = q * pt.NG / pt.P, g1 = (q + 1) * pt.NG / pt.P;
+        const int64_t span = (g1 - 1) / pt.CG - g0 / pt.CG + 1;
+        if (span > J) J = span;
+    }
+    pt.J = J;
+    c->pt = pt;
+    c->lay = make_layout(n, W, c->nchunks, pt.P, pt.J);
+    *out = c;
+    return OB_OK;
+}
+
+void ob_destroy(ob_ctx* c)
+{
+    if (!c) return;
+    for (auto& r : c->recs) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    for (auto e : c->spare) cudaEventDestroy(e);
+    delete c;
+}
+
+size_t ob_workspace_bytes(const ob_ctx* c) { return c ? c->lay.total : 0; }
+
+int ob_workspace_init(ob_ctx* c, void* ws, void* stream)
+{
+    if (!c) return OB_EINVAL;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, c->lay.total, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->has_mask = false;
+    return OB_OK;
+}
+
+int ob_set_lr(ob_ctx* c, float lr)
+{
+    if (!c || !finite(lr)) return OB_EINVAL;
+    c->lr = lr;
+    return OB_OK;
+}
+
+int ob_set_options(ob_ctx* c, float weight_decay, int bias_correction)
+{
+    if (!c || !finite(weight_decay) || weight_decay < 0.0f) return OB_EINVAL;
+    c->wd = weight_decay;
+    c->bias_correction = bias_correction ? 1 : 0;
+    return OB_OK;
+}
+
+int ob_set_step(ob_ctx* c, int64_t step)
+{
+    if (!c || step < 0) return OB_EINVAL;
+    c->step = step;
+    return OB_OK;
+}
+
+int64_t ob_get_step(const ob_ctx* c) { return c ? c->step : -1; }
+
+int ob_set_mask(ob_ctx* c, const float* mask01, void* ws, void* stream)
+{
+    if (!c) return OB_EINVAL;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (mask01 == nullptr) {
+        c->has_mask = false;
+        return OB_OK;
+    }
+    if (int r = check_ptr(mask01, 16)) return r;
+    if (int r = check_device(c)) return r;
+    MaskArgs a{mask01, at<uint32_t>(ws, c->lay.mask), c->n};
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (int r = launch(c, OB_K_MASK, s, [&] { return launch_mask(a, stream_grid(c), s); })) return r;
+    c->has_mask = true;
+    return OB_OK;
+}
+
+int ob_warmup_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, float* v, void* ws,
+                   void* stream)
+{
+    if (!c) return OB_EINVAL;
+    if (int r = check_grads(c, grads, dtype)) return r;
+    for (const void* p : {(const void*)x, (const void*)m, (const void*)v})
+        if (int r = check_ptr(p, 16)) return r;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    const int64_t t = c->step + 1;
+    WarmupArgs a{};
+    a.g = grads;
+    a.x = x;
+    a.m = m;
+    a.v = v;
+    a.n = c->n;
+    a.W = c->W;
+    a.b1 = c->b1;
+    a.c1 = 1.0f - c->b1;
+    a.b2 = c->b2;
+    a.c2 = 1.0f - c->b2;
+    a.eps = c->eps;
+    a.lr = c->lr;
+    a.wd = c->wd;
+    a.bc1 = 1.0f;
+    a.bc2 = 1.0f;
+    a.corrected = 0;
+    if (c->bias_correction) {
+        // (1 - b^t) in double, rounded once to float32
+        a.bc1 = (float)(1.0 - std::pow((double)c->b1, (double)t));
+        a.bc2 = (float)(1.0 - std::pow((double)c->b2, (double)t));
+        a.corrected = (a.bc1 != 1.0f || a.bc2 != 1.0f) ? 1 : 0;
+    }
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (int r = launch(c, OB_K_WARMUP, s, [&] { return launch_warmup(dtype, a, stream_grid(c), s); })) return r;
+    c->step = t;
+    return OB_OK;
+}
+
+int ob_compressed_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, const float* v,
+                       float* worker_err, float* server_err, void* ws, void* stream)
+{
+    if (!c) return OB_EINVAL;
+    if (int r = check_grads(c, grads, dtype)) return r;
+    for (const void* p : {(const void*)x, (const void*)m, (const void*)v, (const void*)worker_err,
+                          (const void*)server_err})
+        if (int r = check_ptr(p, 16)) return r;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const Layout& L = c->lay;
+
+    WorkerArgs wa{};
+    wa.g = grads;
+    wa.m = m;
+    wa.zbuf = worker_err;
+    wa.wbits = at<uint32_t>(ws, L.wbits);
+    wa.s_prev = at<float>(ws, L.s_prev);
+    wa.s_next = at<float>(ws, L.s_next);
+    wa.part = at<double>(ws, L.wpart);
+    wa.cnt = at<unsigned>(ws, L.wcnt);
+    wa.pt = c->pt;
+    wa.n = c->n;
+    wa.C = c->C;
+    wa.b1 = c->b1;
+    wa.c1 = 1.0f - c->b1;
+    const int occ_w = pow2_floor(occupancy_worker(c->W, dtype));
+    const int grid_w = c->sms * (occ_w > 0 ? occ_w : 1);
+    if (int r = launch(c, OB_K_WORKER, s, [&] { return launch_worker(c->W, dtype, wa, grid_w, s); })) return r;
+
+    ServerArgs sa{};
+    sa.wbits = wa.wbits;
+    sa.s_next = wa.s_next;
+    sa.ybuf = server_err;
+    sa.sbits = at<uint32_t>(ws, L.sbits);
+    sa.t_prev = at<float>(ws, L.t_prev);
+    sa.t_next = at<float>(ws, L.t_next);
+    sa.part = at<double>(ws, L.spart);
+    sa.cnt = at<unsigned>(ws, L.scnt);
+    sa.pt = c->pt;
+    sa.n = c->n;
+    sa.C = c->C;
+    const int occ_s = pow2_floor(occupancy_server(c->W));
+    const int grid_s = c->sms * (occ_s > 0 ? occ_s : 1);
+    if (int r = launch(c, OB_K_SERVER, s, [&] { return launch_server(c->W, sa, grid_s, s); })) return r;
+
+    UpdateArgs ua{};
+    ua.sbits = sa.sbits;
+    ua.t_next = sa.t_next;
+    ua.maskbits = c->has_mask ? at<uint32_t>(ws, L.mask) : nullptr;
+    ua.v = v;
+    ua.x = x;
+    ua.m = m;
+    ua.s_prev = at<float>(ws, L.s_prev);
+    ua.s_next = wa.s_next;
+    ua.t_prev = at<float>(ws, L.t_prev);
+    ua.NG = c->pt.NG;
+    ua.CG = c->pt.CG;
+    ua.nscales_w = (int64_t)c->W * c->nchunks;
+    ua.nchunks = c->nchunks;
+    ua.lr = c->lr;
+    ua.eps = c->eps;
+    ua.wd = c->wd;
+    if (int r = launch(c, OB_K_UPDATE, s, [&] { return launch_update(ua, stream_grid(c), s); })) return r;
+    c->step += 1;
+    return OB_OK;
+}
+
+int ob_compressed_step_host(ob_ctx* c, const void* grads_host, void* grads_dev, int dtype, float* x,
+                            float* m, const float* v, float* worker_err, float* server_err, void* ws,
+                            uint32_t* sbits_host, float* sscale_host, void* stream)
+{
+    if (!c || !grads_host || !sbits_host || !sscale_host) return OB_EINVAL;
+    if (int r = check_grads(c, grads_dev, dtype)) return r;
+    for (const void* p : {(const void*)x, (const void*)m, (const void*)v, (const void*)worker_err,
+                          (const void*)server_err})
+        if (int r = check_ptr(p, 16)) return r;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const size_t gbytes = (size_t)c->W * (size_t)c->n * grad_bytes(dtype);
+    cudaError_t e = cudaMemcpyAsync(grads_dev, grads_host, gbytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (int r = ob_compressed_step(c, grads_dev, dtype, x, m, v, worker_err, server_err, ws, stream)) return r;
+    e = cudaMemcpyAsync(sbits_host, at<uint32_t>(ws, c->lay.sbits), (size_t)c->n / 8, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemcpyAsync(sscale_host, at<float>(ws, c->lay.t_next), (size_t)c->nchunks * 4,
+                        cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return OB_OK;
+}
+
+size_t ob_loco_workspace_bytes(const ob_ctx* c, int bits)
+{
+    if (!c || (bits != 4 && bits != 8)) return 0;
+    size_t off = up((size_t)c->W * (size_t)c->n * bits / 8, kAlignWs);   // codes
+    off = up(off + (size_t)c->W * c->nchunks * 4, kAlignWs);               // scales
+    off = up(off + (size_t)c->W * c->nchunks * 4, kAlignWs);               // absmax bits
+    return off;
+}
+
+int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, float* v, float* loco_err,
+                 float beta, int bits, void* loco_ws, void* stream)
+{
+    if (!c) return OB_EINVAL;
+    if (bits != 4 && bits != 8) return OB_ENOTIMPL;
+    if (!finite(beta) || beta < 0.0f || beta > 1.0f) return OB_EINVAL;
+    if (int r = check_grads(c, grads, dtype)) return r;
+    for (const void* p : {(const void*)x, (const void*)m, (const void*)v, (const void*)loco_err})
+        if (int r = check_ptr(p, 16)) return r;
+    if (int r = check_ptr(loco_ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const size_t codes_b = up((size_t)c->W * (size_t)c->n * bits / 8, kAlignWs);
+    const size_t scale_b = up((size_t)c->W * c->nchunks * 4, kAlignWs);
+    LocoArgs a{};
+    a.g = grads;
+    a.err = loco_err;
+    a.codes = at<uint8_t>(loco_ws, 0);
+    a.scale = at<float>(loco_ws, codes_b);
+    a.amax_bits = at<unsigned>(loco_ws, codes_b + scale_b);
+    a.x = x;
+    a.m = m;
+    a.v = v;
+    a.n = c->n;
+    a.C = c->C;
+    a.nchunks = c->nchunks;
+    a.NG = c->n / 256;
+    a.W = c->W;
+    a.bits = bits;
+    a.beta = beta;
+    a.keep = 1.0f - beta;
+    a.b1 = c->b1;
+    a.c1 = 1.0f - c->b1;
+    a.b2 = c->b2;
+    a.c2 = 1.0f - c->b2;
+    a.eps = c->eps;
+    a.lr = c->lr;
+    a.wd = c->wd;
+    const cudaError_t e = cudaMemsetAsync(a.amax_bits, 0, (size_t)c->W * c->nchunks * 4, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int grid = stream_grid(c);
+    if (int r = launch(c, OB_K_LOCO_ABSMAX, s, [&] { return launch_loco_absmax(dtype, a, grid, s); })) return r;
+    if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_quant(dtype, a, grid, s); })) return r;
+    if (int r = launch(c, OB_K_LOCO_SERVER, s, [&] { return launch_loco_server(a, grid, s); })) return r;
+    c->step += 1;
+    return OB_OK;
+}
+
+int ob_reset_errors(ob_ctx* c, float* worker_err, float* server_err, void* ws, void* stream)
+{
+    if (!c) return OB_EINVAL;
+    if (int r = check_ptr(worker_err, 16)) return r;
+    if (int r = check_ptr(server_err, 16)) return r;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const Layout& L = c->lay;
+    cudaError_t e = cudaMemsetAsync(worker_err, 0, (size_t)c->W * c->n * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(server_err, 0, (size_t)c->n * 4, s);
+    // previous and next scales of both sides (contiguous: s_prev .. t_next)
+    if (e == cudaSuccess) e = cudaMemsetAsync(at<char>(ws, L.s_prev), 0, L.wpart - L.s_prev, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return OB_OK;
+}
+
+int ob_export_state(ob_ctx* c, const float* worker_err, const float* server_err, const void* ws,
+                    float* ew_out, float* es_out, void* stream)
+{
+    if (!c) return OB_EINVAL;
+    for (const void* p : {(const void*)worker_err, (const void*)server_err, (const void*)ew_out,
+                          (const void*)es_out})
+        if (int r = check_ptr(p, 16)) return r;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    ExportArgs a{};
+    a.zbuf = worker_err;
+    a.ybuf = server_err;
+    a.s_prev = at<float>(const_cast<void*>(ws), c->lay.s_prev);
+    a.t_prev = at<float>(const_cast<void*>(ws), c->lay.t_prev);
+    a.ew_out = ew_out;
+    a.es_out = es_out;
+    a.n = c->n;
+    a.C = c->C;
+    a.nchunks = c->nchunks;
+    a.W = c->W;
+    const cudaStream_t s = (cudaStream_t)stream;
+    return launch(c, OB_K_EXPORT, s, [&] { return launch_export(a, stream_grid(c), s); });
+}
+
+int ob_debug_views(const ob_ctx* c, const void* ws, const uint32_t** wbits, const float** wscale,
+                   const uint32_t** sbits, const float** sscale)
+{
+    if (!c) return OB_EINVAL;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    void* w = const_cast<void*>(ws);
+    if (wbits) *wbits = at<uint32_t>(w, c->lay.wbits);
+    if (wscale) *wscale = at<float>(w, c->lay.s_next);
+    if (sbits) *sbits = at<uint32_t>(w, c->lay.sbits);
+    if (sscale) *sscale = at<float>(w, c->lay.t_next);
+    return OB_OK;
+}
+
+int ob_profile(ob_ctx* c, int enable)
+{
+    if (!c) return OB_EINVAL;
+    for (auto& r : c->recs) {
+        c->spare.push_back(r.a);
+        c->spare.push_back(r.b);
+    }
+    c->recs.clear();
+    for (int k = 0; k < OB_K_COUNT; ++k) {
+        c->prof_ms[k] = 0.0;
+        c->prof_n[k] = 0;
+    }
+    c->profiling = enable != 0;
+    return OB_OK;
+}
+
+int ob_profile_read(ob_ctx* c, int kernel, double* total_ms, int64_t* launches)
+{
+    if (!c || kernel < 0 || kernel >= OB_K_COUNT) return OB_EINVAL;
+    for (auto& r : c->recs) {
+        const cudaError_t e = cudaEventSynchronize(r.b);
+        if (e != cudaSuccess) return cuda_fail(e);
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+            c->prof_ms[r.kernel] += ms;
+            c->prof_n[r.kernel] += 1;
+        }
+        c->spare.push_back(r.a);
+        c->spare.push_back(r.b);
+    }
+    c->recs.clear();
+    if (total_ms) *total_ms = c->prof_ms[kernel];
+    if (launches) *launches = c->prof_n[kernel];
+    return OB_OK;
+}
+
+int64_t ob_launch_count(const ob_ctx* c) { return c ? c->launches : -1; }
+
+const char* ob_strerror(int code)
+{
+    switch (code) {
+        case OB_OK: return "ok";
+        case OB_EINVAL: return "invalid argument (size, dtype, null pointer or wrong device)";
+        case OB_ECUDA: return "CUDA call or kernel launch failed";
+        case OB_ENOTIMPL: return "not implemented";
+        case OB_EALIGN: return "pointer not aligned (16 bytes; workspace 256 bytes)";
+    }
+    return "unknown status";
+}
+
+int ob_last_cuda_error(void) { return g_last_cuda; }
+
+}  // extern "C"

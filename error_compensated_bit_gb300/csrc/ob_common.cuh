@@ -1,0 +1,223 @@
+// Device helpers shared by the compression-stage kernels (sm_103a).
+//
+// Work decomposition used by every streaming kernel here: the flat buffer is cut into
+// groups of 256 elements (one warp iteration: 8 consecutive elements per lane, i.e. two
+// 16-byte loads of float32 or one 16-byte load of a 16-bit gradient), and the groups
+// into P contiguous ranges of (nearly) equal length, one warp per range. A 256-element
+// group never straddles a chunk (chunk % 256 == 0), so a warp can accumulate a chunk's
+// sum of squares in registers and flush it when its range crosses a chunk boundary.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ob_internal.h"
+
+namespace ob {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---- range partition ---------------------------------------------------------------------
+
+__device__ __forceinline__ int64_t range_begin(const Part& pt, int64_t q)
+{
+    return q * pt.NG / pt.P;
+}
+
+// Ranges that hold at least one group of chunk k: lo..hi inclusive. Every range is
+// non-empty (P <= NG), so this is exactly the set of warps that flush a partial for k.
+__device__ __forceinline__ void chunk_contributors(const Part& pt, int64_t k, int64_t& lo,
+                                                   int64_t& hi)
+{
+    const int64_t a = (k * pt.CG + 1) * pt.P;
+    const int64_t b = (k + 1) * pt.CG * pt.P;
+    lo = (a + pt.NG - 1) / pt.NG - 1;
+    hi = (b + pt.NG - 1) / pt.NG - 1;
+    if (hi > pt.P - 1) hi = pt.P - 1;
+}
+
+// ---- 8-element loads and stores ------------------------------------------------------------
+
+__device__ __forceinline__ void ld8_stream(const float* p, float (&v)[8])
+{
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void st8_stream(float* p, const float (&v)[8])
+{
+    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
+}
+
+// Gradient rows in their storage format, widened exactly to float32.
+template <typename G>
+struct Grad;
+
+template <>
+struct Grad<float> {
+    static __device__ __forceinline__ void ld8(const void* base, int64_t idx, float (&v)[8])
+    {
+        ld8_stream(static_cast<const float*>(base) + idx, v);
+    }
+};
+
+template <>
+struct Grad<__half> {
+    static __device__ __forceinline__ void ld8(const void* base, int64_t idx, float (&v)[8])
+    {
+        const uint4 r = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __half*>(base) + idx));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h;
+            memcpy(&h, &w[i], 4);
+            const float2 f = __half22float2(h);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+};
+
+template <>
+struct Grad<__nv_bfloat16> {
+    static __device__ __forceinline__ void ld8(const void* base, int64_t idx, float (&v)[8])
+    {
+        const uint4 r = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + idx));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {               // bfloat16 is the top half of a float32
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+// ---- sign bits ---------------------------------------------------------------------------------
+
+// Lane `lane` holds the sign bits of elements 8*lane .. 8*lane+7 of a group in `byte`.
+// After the two exchanges, the four lanes of a quad hold the 32-bit word of elements
+// 32*(lane/4) .. 32*(lane/4)+31 (bit t <-> element t of the word).
+__device__ __forceinline__ uint32_t quad_word(uint32_t byte, int lane)
+{
+    uint32_t v = byte << (8 * (lane & 3));
+    v |= __shfl_xor_sync(kFull, v, 1);
+    v |= __shfl_xor_sync(kFull, v, 2);
+    return v;
+}
+
+// The 8 sign bits of this lane's elements inside a row of packed words.
+__device__ __forceinline__ uint32_t lane_byte(const uint32_t* words, int64_t group, int lane)
+{
+    const uint32_t w = __ldcs(words + group * 8 + (lane >> 2));
+    return (w >> (8 * (lane & 3))) & 0xffu;
+}
+
+__device__ __forceinline__ float signed_scale(float s, bool nonneg)
+{
+    return nonneg ? s : -s;
+}
+
+// ---- reductions --------------------------------------------------------------------------------
+
+// Error-free accumulation of squares in float32: every z^2 is split exactly into
+// p + r (p = fl(z*z), r = fma(z, z, -p)) and p is added with Knuth's two-sum, whose
+// rounding error q is exact; the pair (s, e) carries the sum as s + e with an error of
+// order u^2 * terms * sum, which keeps chunk sums within ~1e-12 of an exact double sum.
+struct Sum2 {
+    float s, e;
+};
+
+__device__ __forceinline__ void sum2_add_sq(Sum2& a, float z)
+{
+    const float p = __fmul_rn(z, z);
+    const float r = __fmaf_rn(z, z, -p);
+    const float t = __fadd_rn(a.s, p);
+    const float bp = __fsub_rn(t, a.s);
+    const float ap = __fsub_rn(t, bp);
+    const float q = __fadd_rn(__fsub_rn(a.s, ap), __fsub_rn(p, bp));
+    a.s = t;
+    a.e = __fadd_rn(a.e, __fadd_rn(q, r));
+}
+
+// Butterfly sum: every lane ends with the same, order-fixed value.
+__device__ __forceinline__ double warp_sum(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// A chunk's float32 sum of squares is trusted when its mean square lies in
+// [2^-80, float max): squares of elements below 2^-63 (that underflow in float32) then
+// weigh less than 2^-46 of the total. Otherwise -- an all-zero or all-tiny chunk, or an
+// overflow -- the last contributor recomputes the chunk in double from the stored
+// buffer (a slow path taken only by such degenerate chunks).
+__device__ __forceinline__ bool sumsq_trusted(double sum, int64_t C)
+{
+    return sum >= (double)C * 0x1p-80 && sum <= 0x1p127;
+}
+
+__device__ double chunk_sumsq_exact(const float* row, int64_t C, int lane)
+{
+    double acc = 0.0;
+    for (int64_t i = (int64_t)lane * 4; i < C; i += 128) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(row + i));
+        acc += (double)v.x * v.x;
+        acc += (double)v.y * v.y;
+        acc += (double)v.z * v.z;
+        acc += (double)v.w * v.w;
+    }
+    return warp_sum(acc);
+}
+
+// Flush this warp's sums of squares for chunk k (rows 0..R-1), and, if this warp is
+// the last contributor of chunk k, combine all contributors' partials in ascending
+// range order and write the chunk's RMS scales. No waiting: the last arrival does the
+// work; the counter is reset for the next launch. `rows` is the buffer the squares
+// came from (row r at rows + r*row_stride), read only on the degenerate slow path.
+template <int R>
+__device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int64_t k, int64_t kfirst,
+                                            Sum2 (&acc)[R], double* part, unsigned* cnt,
+                                            float* scale_out, int64_t C, const float* rows,
+                                            int64_t row_stride, int lane)
+{
+    const int64_t j = k - kfirst;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
+        if (lane == 0) part[((int64_t)r * pt.P + q) * pt.J + j] = d;
+        acc[r].s = 0.0f;
+        acc[r].e = 0.0f;
+    }
+    __threadfence();
+    unsigned last = 0;
+    if (lane == 0) {
+        int64_t lo, hi;
+        chunk_contributors(pt, k, lo, hi);
+        const unsigned prev = atomicAdd(cnt + k, 1u);
+        last = (prev == (unsigned)(hi - lo)) ? 1u : 0u;
+    }
+    last = __shfl_sync(kFull, last, 0);
+    if (!last) return;
+    __threadfence();
+    int64_t lo, hi;
+    chunk_contributors(pt, k, lo, hi);
+    for (int r = 0; r < R; ++r) {
+        double sum = 0.0;
+        for (int64_t qq = lo + lane; qq <= hi; qq += 32) {
+            const int64_t jj = k - range_begin(pt, qq) / pt.CG;
+            sum += __ldcg(part + ((int64_t)r * pt.P + qq) * pt.J + jj);
+        }
+        sum = warp_sum(sum);
+        if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
+        if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(sum / (double)C);
+    }
+    if (lane == 0) cnt[k] = 0u;
+}
+
+}  // namespace ob

@@ -1,0 +1,117 @@
+// Internal launch interface between the C ABI (ob_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ob {
+
+// Partition of the buffer into 256-element groups and P contiguous warp ranges.
+struct Part {
+    int64_t NG;       // groups (n / 256)
+    int64_t P;        // ranges (one warp each), 1 <= P <= NG
+    int64_t CG;       // groups per chunk (chunk / 256)
+    int64_t J;        // partial slots per range (most chunks one range touches)
+    int64_t nchunks;  // n / chunk
+};
+
+struct WorkerArgs {
+    const void* g;          // [W][n] gradients
+    const float* m;         // [n] momentum of the previous step
+    float* zbuf;            // [W][n] in: previous z, out: this step's z
+    uint32_t* wbits;        // [W][n/32]
+    const float* s_prev;    // [W][nchunks] scales of the previous step
+    float* s_next;          // [W][nchunks] scales of this step (written by the last contributor)
+    double* part;           // [W][P][J] partial sums of squares
+    unsigned* cnt;          // [nchunks] arrival counters (zero between launches)
+    Part pt;
+    int64_t n, C;
+    float b1, c1;
+};
+
+struct ServerArgs {
+    const uint32_t* wbits;  // [W][n/32]
+    const float* s_next;    // [W][nchunks]
+    float* ybuf;            // [n] in: previous y, out: this step's y
+    uint32_t* sbits;        // [n/32]
+    const float* t_prev;    // [nchunks]
+    float* t_next;          // [nchunks]
+    double* part;           // [P][J]
+    unsigned* cnt;          // [nchunks]
+    Part pt;
+    int64_t n, C;
+};
+
+struct UpdateArgs {
+    const uint32_t* sbits;     // [n/32]
+    const float* t_next;       // [nchunks]
+    const uint32_t* maskbits;  // [n/32] or null
+    const float* v;            // [n] frozen variance
+    float* x;                  // [n]
+    float* m;                  // [n] out
+    float* s_prev;             // [W][nchunks] <- s_next (block 0, after all readers finished)
+    const float* s_next;
+    float* t_prev;             // [nchunks] <- t_next
+    int64_t NG, CG, nscales_w, nchunks;
+    float lr, eps, wd;
+};
+
+struct WarmupArgs {
+    const void* g;  // [W][n]
+    float* x;
+    float* m;
+    float* v;
+    int64_t n;
+    int W;
+    float b1, c1, b2, c2, eps, lr, wd, bc1, bc2;
+    int corrected;
+};
+
+struct MaskArgs {
+    const float* mask01;  // [n]
+    uint32_t* bits;       // [n/32]
+    int64_t n;
+};
+
+struct ExportArgs {
+    const float* zbuf;     // [W][n]
+    const float* ybuf;     // [n]
+    const float* s_prev;   // [W][nchunks]
+    const float* t_prev;   // [nchunks]
+    float* ew_out;         // [W][n]
+    float* es_out;         // [n]
+    int64_t n, C, nchunks;
+    int W;
+};
+
+struct LocoArgs {
+    const void* g;         // [W][n]
+    float* err;            // [W][n] moving average of compensation errors
+    uint8_t* codes;        // [W][n*bits/8]
+    float* scale;          // [W][nchunks]
+    unsigned* amax_bits;   // [W][nchunks] running absmax as float bits (pass 1)
+    float* x;
+    float* m;
+    float* v;
+    int64_t n, C, nchunks, NG;
+    int W, bits;
+    float beta, keep, b1, c1, b2, c2, eps, lr, wd;
+};
+
+// Launchers (return the launch status). `grid` blocks of kBlock threads.
+constexpr int kBlock = 256;
+cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_warmup(int dtype, const WarmupArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_export(const ExportArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_loco_absmax(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s);
+
+// Resident blocks per SM of the worker / server kernel for (W, dtype); 0 on error.
+int occupancy_worker(int W, int dtype);
+int occupancy_server(int W);
+
+}  // namespace ob

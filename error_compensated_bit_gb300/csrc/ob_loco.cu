@@ -1,0 +1,201 @@
+// LoCo low-bit step: each worker compensates its gradient with the moving average of
+// its past compression errors, quantizes it per chunk to signed `bits`-bit levels with
+// an absmax scale, and updates the moving average; the mean of the dequantized
+// gradients then drives a plain Adam step.
+//
+// Method: "LoCo: Low-Bit Communication Adaptor for Large-scale Model Training",
+// "Method" (moving average of historical compensation errors, compensate before
+// compression, then synchronise) and the abstract (compatible with Adam).
+//
+// Three passes. The absmax of c = g + e~ over a chunk must be known before any element
+// of the chunk can be quantized, and a chunk spans up to n/W elements, so c is formed
+// twice (pass 1 for the absmax, pass 2 to quantize) instead of being stored.
+//   pass 1  amax[w][k] = max |g + e~|                (atomicMax on float bits: exact)
+//   pass 2  s = amax/L; q = clamp(rint(c/s), -L, L) (0 when s = 0); e = c - q*s;
+//           e~ = beta*e~ + (1-beta)*e; codes <- q
+//   pass 3  gbar = (sum over w of q_w*s_w)/W; Adam on m, v, x
+// Memory per element: pass 1 W*(grad+4), pass 2 W*(grad+8+bits/8), pass 3
+// W*bits/8 + 24.
+#include "ob_common.cuh"
+
+namespace ob {
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+template <typename G>
+__global__ void __launch_bounds__(kBlock) k_loco_absmax(LocoArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t groups = (int64_t)a.W * a.NG;      // row w's groups follow row w-1's
+    const int64_t CG = a.C / 256;
+    // Consecutive warps take consecutive groups (coalesced); each warp keeps a running
+    // max for the (row, chunk) it is in and publishes it only when that changes, so the
+    // few scale slots see one atomic per warp and chunk rather than one per group.
+    int64_t cur = -1;
+    float run = 0.0f;
+    for (int64_t t = warp; t < groups; t += nwarps) {
+        const int64_t w = t / a.NG, gi = t % a.NG;
+        const int64_t key = w * a.nchunks + gi / CG;
+        if (key != cur) {
+            const float mx = warp_max(run);
+            if (cur >= 0 && lane == 0) atomicMax(a.amax_bits + cur, __float_as_uint(mx));
+            cur = key;
+            run = 0.0f;
+        }
+        const int64_t e0 = gi * 256 + lane * 8;
+        float gv[8], ev[8];
+        Grad<G>::ld8(a.g, w * a.n + e0, gv);
+        ld8_stream(a.err + w * a.n + e0, ev);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) run = fmaxf(run, fabsf(__fadd_rn(gv[j], ev[j])));
+    }
+    const float mx = warp_max(run);
+    if (cur >= 0 && lane == 0) atomicMax(a.amax_bits + cur, __float_as_uint(mx));
+}
+
+template <typename G, int BITS>
+__global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t groups = (int64_t)a.W * a.NG;
+    const int64_t CG = a.C / 256;
+    const float L = (float)((1 << (BITS - 1)) - 1);
+    const int64_t row_bytes = a.n * BITS / 8;
+    for (int64_t t = warp; t < groups; t += nwarps) {
+        const int64_t w = t / a.NG, gi = t % a.NG;
+        const int64_t k = gi / CG;
+        const float s = __fdiv_rn(__uint_as_float(__ldcg(a.amax_bits + w * a.nchunks + k)), L);
+        if (lane == 0 && gi % CG == 0) a.scale[w * a.nchunks + k] = s;
+        const int64_t e0 = gi * 256 + lane * 8;
+        float gv[8], ev[8];
+        Grad<G>::ld8(a.g, w * a.n + e0, gv);
+        ld8_stream(a.err + w * a.n + e0, ev);
+        int qv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float c = __fadd_rn(gv[j], ev[j]);
+            int qi = 0;
+            if (s > 0.0f) {
+                float r = rintf(__fdiv_rn(c, s));
+                r = fminf(fmaxf(r, -L), L);
+                qi = (int)r;
+            }
+            qv[j] = qi;
+            const float e = __fsub_rn(c, __fmul_rn((float)qi, s));
+            ev[j] = __fadd_rn(__fmul_rn(a.beta, ev[j]), __fmul_rn(a.keep, e));
+        }
+        st8_stream(a.err + w * a.n + e0, ev);
+        uint8_t* out = a.codes + w * row_bytes + e0 * BITS / 8;
+        if (BITS == 4) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) word |= ((uint32_t)qv[j] & 0xfu) << (4 * j);
+            __stcs(reinterpret_cast<unsigned int*>(out), word);
+        } else {
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                lo |= ((uint32_t)qv[j] & 0xffu) << (8 * j);
+                hi |= ((uint32_t)qv[j + 4] & 0xffu) << (8 * j);
+            }
+            __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
+        }
+    }
+}
+
+template <int BITS>
+__device__ __forceinline__ void load_codes(const uint8_t* p, int (&q)[8])
+{
+    if (BITS == 4) {
+        const uint32_t word = __ldcs(reinterpret_cast<const unsigned int*>(p));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[j] = ((int)(word << (28 - 4 * j))) >> 28;   // sign-extend nibble j
+    } else {
+        const uint2 r = __ldcs(reinterpret_cast<const uint2*>(p));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            q[j] = ((int)(r.x << (24 - 8 * j))) >> 24;
+            q[j + 4] = ((int)(r.y << (24 - 8 * j))) >> 24;
+        }
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kBlock) k_loco_server(LocoArgs a)
+{
+    const int64_t nvec = a.n / 8;
+    const int64_t row_bytes = a.n * BITS / 8;
+    const float fW = (float)a.W;
+    for (int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i8 < nvec;
+         i8 += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e0 = i8 * 8;
+        const int64_t k = e0 / a.C;
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int w = 0; w < a.W; ++w) {
+            const float s = __ldg(a.scale + (int64_t)w * a.nchunks + k);
+            int q[8];
+            load_codes<BITS>(a.codes + (int64_t)w * row_bytes + e0 * BITS / 8, q);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn((float)q[j], s));
+        }
+        float mv[8], vv[8], xv[8];
+        ld8_stream(a.m + e0, mv);
+        ld8_stream(a.v + e0, vv);
+        ld8_stream(a.x + e0, xv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float gbar = __fdiv_rn(acc[j], fW);
+            mv[j] = __fadd_rn(__fmul_rn(a.b1, mv[j]), __fmul_rn(a.c1, gbar));
+            vv[j] = __fadd_rn(__fmul_rn(a.b2, vv[j]), __fmul_rn(a.c2, __fmul_rn(gbar, gbar)));
+            const float denom = __fadd_rn(__fsqrt_rn(vv[j]), a.eps);
+            float u = __fdiv_rn(mv[j], denom);
+            if (a.wd != 0.0f) u = __fadd_rn(u, __fmul_rn(a.wd, xv[j]));
+            xv[j] = __fsub_rn(xv[j], __fmul_rn(a.lr, u));
+        }
+        st8_stream(a.m + e0, mv);
+        st8_stream(a.v + e0, vv);
+        st8_stream(a.x + e0, xv);
+    }
+}
+
+cudaError_t launch_loco_absmax(int dtype, const LocoArgs& a, int grid, cudaStream_t s)
+{
+    if (dtype == 0) k_loco_absmax<float><<<grid, kBlock, 0, s>>>(a);
+    else if (dtype == 1) k_loco_absmax<__half><<<grid, kBlock, 0, s>>>(a);
+    else k_loco_absmax<__nv_bfloat16><<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream_t s)
+{
+    if (a.bits == 4) {
+        if (dtype == 0) k_loco_quant<float, 4><<<grid, kBlock, 0, s>>>(a);
+        else if (dtype == 1) k_loco_quant<__half, 4><<<grid, kBlock, 0, s>>>(a);
+        else k_loco_quant<__nv_bfloat16, 4><<<grid, kBlock, 0, s>>>(a);
+    } else {
+        if (dtype == 0) k_loco_quant<float, 8><<<grid, kBlock, 0, s>>>(a);
+        else if (dtype == 1) k_loco_quant<__half, 8><<<grid, kBlock, 0, s>>>(a);
+        else k_loco_quant<__nv_bfloat16, 8><<<grid, kBlock, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s)
+{
+    if (a.bits == 4) k_loco_server<4><<<grid, kBlock, 0, s>>>(a);
+    else k_loco_server<8><<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ob

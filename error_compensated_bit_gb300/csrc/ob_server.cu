@@ -1,0 +1,206 @@
+// Server side of the compression-stage step and the final update.
+//
+// Method: DeepSpeed 1-bit Adam training guide, §4 (compressed_allreduce: a server_error
+// per GPU, the averaged momentum recompressed and sent back; then
+// update = exp_avg/(sqrt(exp_avg_sq)+eps), weight decay and learning rate), §3.5
+// (exp_avg multiplied by exp_avg_mask after the exchange); "1-bit Adam" review,
+// "Proposed method" (the variance frozen after the warm-up preconditions the update).
+//
+// The exchange is a gather inside device memory: the server pass reads, for its
+// elements, every worker's packed words (the all-to-all), and the update pass reads
+// the server's words (the all-gather). Nothing is copied.
+#include "ob_common.cuh"
+
+namespace ob {
+
+// a = (sum over w ascending of +-S_wk)/W;  e_s = yprev - T_prev*sign(yprev);  y = a + e_s;
+// bit = (y >= 0); ybuf = y; chunk sums of y^2 -> T_next.
+// Memory per element: W/8 (worker bits) + 4 + 4 (y) + 1/8 (server bits).
+template <int W>
+__global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const Part pt = a.pt;
+    const int64_t words_per_row = a.n / 32;
+    const float fW = (float)W;
+
+    for (int64_t q = warp; q < pt.P; q += nwarps) {
+        const int64_t g0 = range_begin(pt, q);
+        const int64_t g1 = range_begin(pt, q + 1);
+        int64_t k = g0 / pt.CG;
+        const int64_t kfirst = k;
+        int64_t kend = (k + 1) * pt.CG;
+
+        float sw[W];
+#pragma unroll
+        for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
+        float tp = __ldg(a.t_prev + k);
+        Sum2 acc[1] = {{0.0f, 0.0f}};
+
+        for (int64_t gi = g0; gi < g1; ++gi) {
+            if (gi == kend) {
+                flush_chunk<1>(pt, q, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+                ++k;
+                kend += pt.CG;
+#pragma unroll
+                for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
+                tp = __ldg(a.t_prev + k);
+            }
+            uint32_t bytes[W];
+#pragma unroll
+            for (int w = 0; w < W; ++w) bytes[w] = lane_byte(a.wbits + (int64_t)w * words_per_row, gi, lane);
+            const int64_t e0 = gi * 256 + lane * 8;
+            float yv[8];
+            ld8_stream(a.ybuf + e0, yv);
+            uint32_t byte = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) sum = __fadd_rn(sum, signed_scale(sw[w], (bytes[w] >> j) & 1u));
+                const float avg = __fdiv_rn(sum, fW);
+                const float es = __fsub_rn(yv[j], signed_scale(tp, yv[j] >= 0.0f));
+                const float y = __fadd_rn(avg, es);
+                yv[j] = y;
+                byte |= (y >= 0.0f ? 1u : 0u) << j;
+                sum2_add_sq(acc[0], y);
+            }
+            st8_stream(a.ybuf + e0, yv);
+            const uint32_t word = quad_word(byte, lane);
+            if ((lane & 3) == 0) __stcs(a.sbits + gi * 8 + (lane >> 2), word);
+        }
+        flush_chunk<1>(pt, q, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+    }
+}
+
+// m = T_k*sign(y) [* mask];  x -= lr*(m/(sqrt(v)+eps) [+ wd*x]).
+// Memory per element: 1/8 (server bits) [+ 1/8 mask bits] + 4 (v) + 8 (x) + 4 (m).
+// Block 0 also moves this step's scales into the "previous" slots for the next step:
+// every kernel that reads the previous slots (worker, server) has finished by now.
+__global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const bool masked = a.maskbits != nullptr;
+
+    for (int64_t gi = warp; gi < a.NG; gi += nwarps) {
+        const float T = __ldg(a.t_next + gi / a.CG);
+        const uint32_t sb = lane_byte(a.sbits, gi, lane);
+        const uint32_t mb = masked ? lane_byte(a.maskbits, gi, lane) : 0xffu;
+        const int64_t e0 = gi * 256 + lane * 8;
+        float vv[8], xv[8], mv[8];
+        ld8_stream(a.v + e0, vv);
+        ld8_stream(a.x + e0, xv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float mi = signed_scale(T, (sb >> j) & 1u);
+            if (masked) mi = __fmul_rn(mi, ((mb >> j) & 1u) ? 1.0f : 0.0f);
+            mv[j] = mi;
+            const float denom = __fadd_rn(__fsqrt_rn(vv[j]), a.eps);
+            float u = __fdiv_rn(mi, denom);
+            if (a.wd != 0.0f) u = __fadd_rn(u, __fmul_rn(a.wd, xv[j]));
+            xv[j] = __fsub_rn(xv[j], __fmul_rn(a.lr, u));
+        }
+        st8_stream(a.m + e0, mv);
+        st8_stream(a.x + e0, xv);
+    }
+
+    if (blockIdx.x == 0) {
+        for (int64_t i = threadIdx.x; i < a.nscales_w; i += blockDim.x) a.s_prev[i] = a.s_next[i];
+        for (int64_t i = threadIdx.x; i < a.nchunks; i += blockDim.x) a.t_prev[i] = a.t_next[i];
+    }
+}
+
+// Momentum mask (float 0/1) -> packed bits, bit = (mask != 0).
+__global__ void __launch_bounds__(kBlock) k_mask(MaskArgs a)
+{
+    const int64_t nwords = a.n / 32;
+    for (int64_t wi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; wi < nwords;
+         wi += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t word = 0;
+        for (int t = 0; t < 32; ++t) word |= (a.mask01[wi * 32 + t] != 0.0f ? 1u : 0u) << t;
+        a.bits[wi] = word;
+    }
+}
+
+// True residuals from the stored (z, S) and (y, T): e = z - S*sign(z).
+__global__ void __launch_bounds__(kBlock) k_export(ExportArgs a)
+{
+    const int64_t total = (int64_t)(a.W + 1) * a.n;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t w = i / a.n, e = i % a.n;
+        const int64_t k = e / a.C;
+        if (w < a.W) {
+            const float z = a.zbuf[i];
+            a.ew_out[i] = __fsub_rn(z, signed_scale(a.s_prev[w * a.nchunks + k], z >= 0.0f));
+        } else {
+            const float y = a.ybuf[e];
+            a.es_out[e] = __fsub_rn(y, signed_scale(a.t_prev[k], y >= 0.0f));
+        }
+    }
+}
+
+template <int W>
+static cudaError_t launch_s(const ServerArgs& a, int grid, cudaStream_t s)
+{
+    k_server<W><<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int W>
+static int occ_s()
+{
+    int blocks = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_server<W>, kBlock, 0) == cudaSuccess
+               ? blocks : 0;
+}
+
+#define OB_FOR_EACH_W(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(16)
+
+cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s)
+{
+    switch (W) {
+#define OB_CASE(w) \
+    case w:        \
+        return launch_s<w>(a, grid, s);
+        OB_FOR_EACH_W(OB_CASE)
+#undef OB_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+int occupancy_server(int W)
+{
+    switch (W) {
+#define OB_CASE(w) \
+    case w:        \
+        return occ_s<w>();
+        OB_FOR_EACH_W(OB_CASE)
+#undef OB_CASE
+    }
+    return 0;
+}
+
+cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s)
+{
+    k_update<<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s)
+{
+    k_mask<<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_export(const ExportArgs& a, int grid, cudaStream_t s)
+{
+    k_export<<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ob

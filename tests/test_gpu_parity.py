@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle, element by
+element, on the same seeded inputs. Sign words bit-exact; float32 state within
+1e-7 + 1e-5*|oracle| (see gpu_util for the tie-margin rule of multi-step runs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_util import GpuRun, Tracker, assert_close, exact_fraction, random_state, unpack_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from error_compensated_bit_gb300 import build
+    build.build()
+
+
+def _grads(rng, W, n, dtype, scale=1e-3):
+    g = (rng.standard_normal((W, n)) * scale).astype(np.float32)
+    if dtype == "f16":
+        return g.astype(np.float16)
+    if dtype == "bf16":
+        return (g.view(np.uint32) >> 16).astype(np.uint16)     # truncated to bfloat16
+    return g
+
+
+def _free_run(ora, st, grads_fn, steps, mask=None):
+    gpu = GpuRun(st, mask=mask)
+    tr = Tracker(st.n, st.W, st.C)
+    fracs = []
+    for t in range(steps):
+        g = grads_fn(t)
+        out = ora.compressed_step(st, g)
+        gpu.compressed_step(g)
+        snap = gpu.snapshot()
+        tr.compare(t, snap, out, st, check_mask=mask)
+        fracs.append(exact_fraction(snap, out, st))
+    return tr, fracs
+
+
+def test_tiny_workload_ten_steps(ora):
+    """The tiny workload: n = 2^20, W = 4, chunk = n/W, float32 grads, 10 steps."""
+    from error_compensated_bit_gb300 import synth
+    wl = synth.workload("tiny")
+    st = O.OracleState(wl.n, wl.W, wl.C, x=synth.params(wl).numpy(), m=np.zeros(wl.n),
+                       v=synth.variance(wl).numpy(), b1=wl.b1, b2=wl.b2, eps=wl.eps, lr=wl.lr)
+    tr, fracs = _free_run(ora, st, lambda t: synth.to_numpy_grads(synth.grads(wl, t)), wl.steps)
+    print("tiny: %d sign flips at %d near-ties; bit-identical float fraction per step %s"
+          % (tr.flips, tr.near_ties, ["%.6f" % f for f in fracs]))
+    assert tr.flips <= 2
+
+
+# (W, grad dtype, groups of 256 per worker row, groups per chunk): ragged partitions
+# (the group count is not a multiple of the warp count), several chunks per worker,
+# chunk = 256 (every group its own chunk), one chunk per worker, prime sizes.
+CASES = [
+    (1, "f32", 64, 64),
+    (2, "f16", 300, 100),
+    (3, "bf16", 777, 259),
+    (4, "f32", 1000, 1),
+    (5, "bf16", 600, 600),
+    (8, "f16", 1000, 250),
+    (8, "f32", 1234, 617),
+    (16, "f32", 173, 173),
+    (16, "bf16", 96, 8),
+    (7, "f16", 2000, 400),
+]
+
+
+@pytest.mark.parametrize("W,dtype,groups,cgroups", CASES)
+def test_compressed_step_parity(ora, W, dtype, groups, cgroups):
+    rng = np.random.default_rng(1000 + W * 7 + groups)
+    n = W * 256 * groups
+    C = 256 * cgroups
+    st = random_state(rng, n, W, C, lr=1e-4)
+    tr, fracs = _free_run(ora, st, lambda t: _grads(rng, W, n, dtype), 4)
+    print("W=%d %s: %d sign flips at %d near-ties; bit-identical float fraction %s"
+          % (W, dtype, tr.flips, tr.near_ties, ["%.6f" % f for f in fracs]))
+    assert tr.flips <= 2
+
+
+def test_momentum_mask_parity(ora):
+    """BERT-Base-like: 2% of positions have exactly-zero gradients and a zero mask."""
+    rng = np.random.default_rng(77)
+    W, n = 8, 8 * 256 * 700
+    C = n // W
+    zero = rng.random(n) < 0.02
+    mask = (~zero).astype(np.float32)
+    st = random_state(rng, n, W, C, v_dist="lognormal", mask=mask)
+
+    def grads(t):
+        g = _grads(rng, W, n, "f32")
+        g[:, zero] = 0.0
+        return g
+    tr, _ = _free_run(ora, st, grads, 5, mask=mask)
+
+
+def test_weight_decay_parity(ora):
+    rng = np.random.default_rng(78)
+    W, n = 4, 4 * 256 * 300
+    st = random_state(rng, n, W, n // W, wd=0.01, lr=4e-4)
+    _free_run(ora, st, lambda t: _grads(rng, W, n, "f16"), 3)
+
+
+@pytest.mark.parametrize("case", ["zeros", "negzero", "single", "negative", "subnormal",
+                                  "mask_all_zero", "huge_range"])
+def test_edge_cases(ora, case):
+    rng = np.random.default_rng(5)
+    W, n = 4, 4 * 256 * 64
+    C = 256 * 16
+    mask = None
+    st = random_state(rng, n, W, C)
+    g = np.zeros((W, n), np.float32)
+    if case == "zeros":
+        st.x[:] = 0.0
+    elif case == "negzero":
+        g[:] = -0.0
+    elif case == "single":
+        g[2, 12345] = 1e-3
+    elif case == "negative":
+        g[:] = -np.abs(_grads(rng, W, n, "f32"))
+    elif case == "subnormal":
+        g[:] = np.float32(1e-41) * rng.choice([-1.0, 1.0], (W, n)).astype(np.float32)
+    elif case == "mask_all_zero":
+        g = _grads(rng, W, n, "f32")
+        mask = np.zeros(n, np.float32)
+        st.mask = np.zeros(n, np.uint8)
+    elif case == "huge_range":
+        g = _grads(rng, W, n, "f32") * np.float32(10.0) ** rng.integers(-12, 6, (W, n)).astype(np.float32)
+    gpu = GpuRun(st, mask=mask)
+    tr = Tracker(n, W, C)
+    for t in range(3):
+        out = ora.compressed_step(st, g)
+        gpu.compressed_step(g)
+        tr.compare(t, gpu.snapshot(), out, st, check_mask=mask)
+    if case in ("zeros", "negzero"):
+        snap = gpu.snapshot()
+        assert np.all(snap["wbits"] == 0xFFFFFFFF) and np.all(snap["wscale"] == 0)
+
+
+def test_deterministic(ora):
+    rng = np.random.default_rng(9)
+    W, n = 8, 8 * 256 * 500
+    st = random_state(rng, n, W, n // W)
+    g = _grads(rng, W, n, "f16")
+    snaps = []
+    for rep in range(2):
+        gpu = GpuRun(st.copy())
+        for t in range(3):
+            gpu.compressed_step(g)
+        snaps.append(gpu.snapshot())
+    for k in snaps[0]:
+        assert np.array_equal(np.asarray(snaps[0][k]).view(np.uint8), np.asarray(snaps[1][k]).view(np.uint8)), k
+
+
+def test_reset_and_export(ora):
+    """Errors reset as on checkpoint load: the next step equals one from zero errors."""
+    rng = np.random.default_rng(10)
+    W, n = 4, 4 * 256 * 200
+    C = n // W // 2
+    st = random_state(rng, n, W, C)
+    gpu = GpuRun(st)
+    tr = Tracker(n, W, C)
+    for t in range(2):
+        g = _grads(rng, W, n, "f32")
+        out = ora.compressed_step(st, g)
+        gpu.compressed_step(g)
+        tr.compare(t, gpu.snapshot(), out, st)
+    gpu.ctx.reset_errors(gpu.ew, gpu.es, gpu.ws)
+    ew, es = gpu.errors()
+    assert not ew.any() and not es.any()
+    st.ew[:] = 0.0
+    st.es[:] = 0.0
+    g = _grads(rng, W, n, "f32")
+    out = ora.compressed_step(st, g)
+    gpu.compressed_step(g)
+    tr.compare(2, gpu.snapshot(), out, st)
+
+
+@pytest.mark.parametrize("W,dtype,bc,wd", [(8, "f32", False, 0.0), (4, "f16", True, 0.01),
+                                           (3, "bf16", True, 0.0), (1, "f32", False, 0.01)])
+def test_warmup_parity(ora, W, dtype, bc, wd):
+    rng = np.random.default_rng(20 + W)
+    n = W * 256 * 333
+    st = random_state(rng, n, W, n // W, v_dist="lognormal", wd=wd)
+    gpu = GpuRun(st)
+    gpu.ctx.set_options(wd, bc)
+    for t in range(4):
+        g = _grads(rng, W, n, dtype)
+        ora.warmup_step(st, g, bias_correction=bc)
+        gpu.warmup_step(g)
+        torch.cuda.synchronize()
+        assert_close("warm-up %d m" % t, gpu.m.cpu().numpy(), st.m)
+        assert_close("warm-up %d v" % t, gpu.v.cpu().numpy(), st.v)
+        assert_close("warm-up %d x" % t, gpu.x.cpu().numpy(), st.x)
+    assert np.array_equal(gpu.x.cpu().numpy(), st.x), "warm-up is element-wise: bit-exact"
+
+
+def test_warmup_then_compressed(ora):
+    """The BERT-Base recipe in small: warm-up steps, then compressed steps with a mask."""
+    rng = np.random.default_rng(31)
+    W, n = 8, 8 * 256 * 250
+    zero = rng.random(n) < 0.02
+    mask = (~zero).astype(np.float32)
+    st = random_state(rng, n, W, n // W, v_dist="lognormal", mask=mask)
+    gpu = GpuRun(st, mask=mask)
+    tr = Tracker(n, W, n // W)
+    for t in range(7):
+        g = _grads(rng, W, n, "f32")
+        g[:, zero] = 0.0
+        if t < 3:
+            ora.warmup_step(st, g)
+            gpu.warmup_step(g)
+        else:
+            out = ora.compressed_step(st, g)
+            gpu.compressed_step(g)
+            tr.compare(t, gpu.snapshot(), out, st, check_mask=mask)
+
+
+@pytest.mark.parametrize("W,dtype,bits", [(4, "bf16", 4), (2, "f32", 8), (3, "f16", 4)])
+def test_loco_parity(ora, W, dtype, bits):
+    from error_compensated_bit_gb300 import ob
+    rng = np.random.default_rng(40 + W)
+    n = W * 256 * 400
+    C = n // W // 2
+    st = random_state(rng, n, W, C)
+    st.v[:] = 0.0
+    gpu = GpuRun(st)
+    err_d = torch.zeros(W, n, dtype=torch.float32, device="cuda")
+    lws = torch.zeros(gpu.ctx.loco_workspace_bytes(bits), dtype=torch.uint8, device="cuda")
+    err = np.zeros((W, n), np.float32)
+    code_bytes = W * n * bits // 8
+    scale_off = (code_bytes + 255) // 256 * 256
+    for t in range(4):
+        g = _grads(rng, W, n, dtype)
+        out = ora.loco_step(st, g, err, beta=0.9, bits=bits)
+        from gpu_util import to_device_grads
+        gpu.ctx.loco_step(to_device_grads(g, "cuda"), gpu.x, gpu.m, gpu.v, err_d, lws, 0.9, bits)
+        torch.cuda.synchronize()
+        codes = lws[:code_bytes].cpu().numpy().reshape(W, -1)
+        scales = lws[scale_off:scale_off + W * (n // C) * 4].view(torch.float32).cpu().numpy().reshape(W, -1)
+        assert np.array_equal(codes, out["codes"]), "step %d codes" % t
+        assert np.array_equal(scales, out["scales"]), "step %d scales" % t
+        assert_close("loco %d err" % t, err_d.cpu().numpy(), err)
+        assert_close("loco %d m" % t, gpu.m.cpu().numpy(), st.m)
+        assert_close("loco %d v" % t, gpu.v.cpu().numpy(), st.v)
+        assert_close("loco %d x" % t, gpu.x.cpu().numpy(), st.x)
+    assert np.array_equal(err_d.cpu().numpy(), err), "LoCo has no sums: bit-exact"
+
+
+def test_stream_ordering():
+    """Calls are asynchronous on the given stream: a step enqueued on a side stream is
+    ordered after work already on that stream and visible after synchronizing it."""
+    from error_compensated_bit_gb300.optimizer import OneBitAdam
+    rng = np.random.default_rng(50)
+    W, n = 2, 2 * 256 * 64
+    opt = OneBitAdam(n, W, freeze_step=0)
+    side = torch.cuda.Stream()
+    g = torch.from_numpy(_grads(rng, W, n, "f32")).cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        g.mul_(2.0)              # queued on the side stream before the step
+        opt.step(g)
+    side.synchronize()
+    ref = OneBitAdam(n, W, freeze_step=0)
+    ref.step(g)
+    torch.cuda.synchronize()
+    assert torch.equal(opt.x, ref.x) and torch.equal(opt.m, ref.m)
