@@ -162,7 +162,7 @@ __device__ __forceinline__ bool sumsq_trusted(double sum, int64_t C)
     return sum >= (double)C * 0x1p-80 && sum <= 0x1p127;
 }
 
-__device__ double chunk_sumsq_exact(const float* row, int64_t C, int lane)
+static __device__ __noinline__ double chunk_sumsq_exact(const float* row, int64_t C, int lane)
 {
     double acc = 0.0;
     for (int64_t i = (int64_t)lane * 4; i < C; i += 128) {
