@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -573,6 +574,7 @@ const char* ob_strerror(int code)
         case OB_ECUDA: return "CUDA call or kernel launch failed";
         case OB_ENOTIMPL: return "not implemented";
         case OB_EALIGN: return "pointer not aligned (16 bytes; workspace 256 bytes)";
+        case OB_ESCRATCH: return "too large for the fixed no-allocation scratch (OB_NOALLOC_SCRATCH_BYTES)";
     }
     return "unknown status";
 }
@@ -580,3 +582,81 @@ const char* ob_strerror(int code)
 int ob_last_cuda_error(void) { return g_last_cuda; }
 
 }  // extern "C"
+
+// ---- worker pass without any allocation ------------------------------------------------------
+//
+// For callers that cannot allocate device memory (inside a stream capture, or behind a
+// runtime that owns all device memory): the worker kernel's scratch -- per-range partial
+// sums and per-chunk arrival counters -- lives in this fixed array instead of a
+// caller-provided workspace. Every GPU that loads the library holds the array until the
+// process exits. Host code may not use the array's name as an address: it only stands
+// for the symbol there, so the device address is looked up once per device, with that
+// device current, by cudaGetSymbolAddress.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[OB_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on `dev` (which must be current); looked up on the
+// first call for that device and remembered.
+int noalloc_scratch(int dev, void** out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return OB_EINVAL;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return OB_OK;
+}
+
+}  // namespace
+
+extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtype, const float* m,
+                                          float* worker_err, const float* scale_prev, uint32_t* wbits,
+                                          float* scale_out, void* stream)
+{
+    if (!c) return OB_EINVAL;
+    if (int r = check_grads(c, grads, dtype)) return r;
+    for (const void* p : {(const void*)m, (const void*)worker_err, (const void*)scale_prev,
+                          (const void*)wbits, (const void*)scale_out})
+        if (int r = check_ptr(p, 16)) return r;
+    if (scale_prev == scale_out) return OB_EINVAL;
+    // scratch: partial sums [W][P][J] doubles, then one counter per chunk
+    const size_t part_bytes = up((size_t)c->W * c->pt.P * c->pt.J * 8, kAlignWs);
+    const size_t cnt_bytes = (size_t)c->nchunks * 4;
+    if (part_bytes + cnt_bytes > (size_t)OB_NOALLOC_SCRATCH_BYTES) return OB_ESCRATCH;
+    if (int r = check_device(c)) return r;
+    void* scratch = nullptr;
+    if (int r = noalloc_scratch(c->device, &scratch)) return r;
+    const cudaStream_t s = (cudaStream_t)stream;
+    unsigned* cnt = at<unsigned>(scratch, part_bytes);
+    // the counters must start at zero; the partials are written before they are read
+    const cudaError_t e = cudaMemsetAsync(cnt, 0, cnt_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    WorkerArgs wa{};
+    wa.g = grads;
+    wa.m = m;
+    wa.zbuf = worker_err;
+    wa.wbits = wbits;
+    wa.s_prev = scale_prev;
+    wa.s_next = scale_out;
+    wa.part = at<double>(scratch, 0);
+    wa.cnt = cnt;
+    wa.pt = c->pt;
+    wa.n = c->n;
+    wa.C = c->C;
+    wa.b1 = c->b1;
+    wa.c1 = 1.0f - c->b1;
+    const int occ_w = pow2_floor(occupancy_worker(c->W, dtype));
+    const int grid_w = c->sms * (occ_w > 0 ? occ_w : 1);
+    return launch(c, OB_K_WORKER, s, [&] { return launch_worker(c->W, dtype, wa, grid_w, s); });
+}

@@ -13,7 +13,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libob.so")
 
-OB_OK, OB_EINVAL, OB_ECUDA, OB_ENOTIMPL, OB_EALIGN = 0, -1, -2, -3, -4
+OB_OK, OB_EINVAL, OB_ECUDA, OB_ENOTIMPL, OB_EALIGN, OB_ESCRATCH = 0, -1, -2, -3, -4, -5
+OB_NOALLOC_SCRATCH_BYTES = 4 << 20
 OB_F32, OB_F16, OB_BF16 = 0, 1, 2
 (OB_K_WORKER, OB_K_SERVER, OB_K_UPDATE, OB_K_WARMUP, OB_K_LOCO_ABSMAX, OB_K_LOCO_QUANT,
  OB_K_LOCO_SERVER, OB_K_MASK, OB_K_EXPORT, OB_K_COUNT) = range(10)
@@ -51,6 +52,7 @@ SIGNATURES = {
     "ob_launch_count": (_i64, [_vp]),
     "ob_strerror": (ctypes.c_char_p, [_int]),
     "ob_last_cuda_error": (_int, []),
+    "ob_worker_compress_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 _LIB = None
@@ -202,3 +204,9 @@ class Context:
 
     def launch_count(self):
         return int(_lib().ob_launch_count(self.h))
+
+    def worker_compress_noalloc(self, grads, m, worker_err, scale_prev, wbits, scale_out,
+                                stream=None):
+        """The worker pass with its scratch in the library's fixed array (no workspace)."""
+        _call("ob_worker_compress_noalloc", self.h, _ptr(grads), dtype_code(grads), _ptr(m),
+              _ptr(worker_err), _ptr(scale_prev), _ptr(wbits), _ptr(scale_out), _stream(stream))

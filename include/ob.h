@@ -71,7 +71,8 @@ enum {
     OB_EINVAL = -1,   /* bad size, dtype, NULL pointer, or wrong device current */
     OB_ECUDA = -2,    /* a CUDA call or launch failed; ob_last_cuda_error() has the code */
     OB_ENOTIMPL = -3, /* valid request that this library does not implement */
-    OB_EALIGN = -4    /* a pointer is not aligned as required */
+    OB_EALIGN = -4,   /* a pointer is not aligned as required */
+    OB_ESCRATCH = -5  /* problem too large for the fixed no-allocation scratch array */
 };
 
 enum { OB_F32 = 0, OB_F16 = 1, OB_BF16 = 2 };   /* gradient storage formats */
@@ -229,6 +230,47 @@ int64_t ob_launch_count(const ob_ctx *ctx);
 /* Text for a status code; the last CUDA error number seen by this thread. */
 const char *ob_strerror(int code);
 int ob_last_cuda_error(void);
+
+/* ---- a worker pass that allocates nothing ------------------------------------------------ */
+
+/*
+ * For callers that cannot allocate device memory at all -- code that runs while a
+ * stream is being captured into a CUDA graph (where cudaMalloc is not allowed), or a
+ * host runtime that hands out every byte of device memory from its own arena and has
+ * no room for a separate workspace.
+ *
+ * The pages have no counterpart of this entry point: it is a packaging of the worker
+ * pass of ob_compressed_step (momentum, error compensation, sign packing and chunk
+ * scales, the first of that step's three kernels), running the same kernel with the
+ * same launch shape, so its outputs are bit-identical to that pass's.
+ *
+ * The caller passes every input and output; only the kernel's scratch (one double per
+ * warp range, row and touched chunk, plus one arrival counter per chunk) lives in a
+ * fixed array of OB_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
+ * that loads the library keeps until the process exits. Sizes whose scratch would not
+ * fit -- many tiny chunks over a large buffer -- return OB_ESCRATCH and enqueue nothing.
+ * The call itself never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ *   grads        [W][n] in dtype                    (input)
+ *   m            [n] momentum of the previous step   (input)
+ *   worker_err   [W][n] previous z in, this step's z out (the representation described
+ *                at the top of this file)
+ *   scale_prev   [W][n/chunk] scales of the previous step (input; zeros at the start)
+ *   wbits        [W][n/32] packed signs               (output)
+ *   scale_out    [W][n/chunk] this step's scales      (output; must not alias scale_prev)
+ *
+ * The scratch array is shared by every call in the process: calls whose kernels could
+ * run at the same time on the GPU (different streams, or different host threads) race
+ * on it and must be serialized by the caller. Each call clears the counters it needs
+ * before its kernel runs; the rest of the array keeps whatever the last call left.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make that first call before any
+ * stream capture begins.
+ */
+#define OB_NOALLOC_SCRATCH_BYTES (4u << 20)
+int ob_worker_compress_noalloc(ob_ctx *ctx, const void *grads, int dtype, const float *m,
+                               float *worker_err, const float *scale_prev, uint32_t *wbits,
+                               float *scale_out, void *stream);
 
 #ifdef __cplusplus
 }
