@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--workload", default="bertL", choices=["tiny", "bertB", "bertL", "sweep", "loco"])
     p.add_argument("--phase", default="compressed", choices=["compressed", "warmup", "loco"])
     p.add_argument("--W", type=int, default=None, help="workers (sweep workload)")
+    p.add_argument("--n", type=int, default=None,
+                   help="elements (default: the workload's own size; smaller cases are for profiling)")
+    p.add_argument("--chunk", type=int, default=None, help="elements per scale (default n/W)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -350,7 +353,7 @@ def gpu_arm(args, wl):
 
     # end to end through the host-buffer entry point (compressed phase only)
     e2e = None
-    if args.phase == "compressed":
+    if args.phase == "compressed" and args.e2e_steps > 0:
         g_host = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
         g_host.copy_(g)
         sb_host = torch.empty(n // 32, dtype=torch.int32, pin_memory=True)
@@ -409,7 +412,7 @@ def gpu_arm(args, wl):
 def main():
     args = parse()
     from error_compensated_bit_gb300 import synth
-    wl = synth.workload(args.workload, W=args.W)
+    wl = synth.workload(args.workload, W=args.W, n=args.n, chunk=args.chunk)
     if args.phase == "loco" and args.workload != "loco":
         pass
     if args.impl == "reference":

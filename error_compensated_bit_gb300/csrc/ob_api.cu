@@ -22,7 +22,7 @@ constexpr int kWarpsPerBlock = kBlock / 32;
 size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t wbits, sbits, mask, s_prev, s_next, t_prev, t_next, wpart, spart, wcnt, scnt, total;
+    size_t wbits, sbits, mask, s_prev, s_next, t_prev, t_next, wpart, spart, wcnt, scnt, status, total;
 };
 
 struct Rec {
@@ -40,7 +40,10 @@ struct ob_ctx {
     int64_t step = 0;
     int device = -1;
     int sms = 152;
-    Part pt{};
+    int smem_budget = 232448;   // opt-in shared memory per block
+    Part ptw[3]{};              // worker partition per gradient type (one warp per range)
+    Part pts{};                 // server partition
+    int grid_s = 0;
     Layout lay{};
     bool has_mask = false;
     int64_t launches = 0;
@@ -118,7 +121,7 @@ int pow2_floor(int v)
     return v < 1 ? 1 : p;
 }
 
-Layout make_layout(int64_t n, int W, int64_t nch, int64_t P, int64_t J)
+Layout make_layout(int64_t n, int W, int64_t nch, int64_t wpart_doubles, int64_t spart_doubles)
 {
     Layout L{};
     size_t off = 0;
@@ -134,10 +137,11 @@ Layout make_layout(int64_t n, int W, int64_t nch, int64_t P, int64_t J)
     L.s_next = take((size_t)W * nch * 4);
     L.t_prev = take((size_t)nch * 4);
     L.t_next = take((size_t)nch * 4);
-    L.wpart = take((size_t)W * P * J * 8);
-    L.spart = take((size_t)P * J * 8);
+    L.wpart = take((size_t)wpart_doubles * 8);
+    L.spart = take((size_t)spart_doubles * 8);
     L.wcnt = take((size_t)nch * 4);
     L.scnt = take((size_t)nch * 4);
+    L.status = take(4);
     L.total = off;
     return L;
 }
@@ -155,6 +159,25 @@ int check_grads(const ob_ctx* c, const void* g, int dtype)
 }
 
 int grad_bytes(int dtype) { return dtype == OB_F32 ? 4 : 2; }
+
+// P contiguous ranges of 256-element groups (at most one per group), and J, the most
+// chunks any one range touches.
+Part make_part(int64_t n, int64_t chunk, int64_t want)
+{
+    Part pt{};
+    pt.NG = n / 256;
+    pt.CG = chunk / 256;
+    pt.nchunks = n / chunk;
+    pt.P = want < pt.NG ? (want < 1 ? 1 : want) : pt.NG;
+    int64_t J = 1;
+    for (int64_t q = 0; q < pt.P; ++q) {
+        const int64_t g0 = q * pt.NG / pt.P, g1 = (q + 1) * pt.NG / pt.P;
+        const int64_t span = (g1 - 1) / pt.CG - g0 / pt.CG + 1;
+        if (span > J) J = span;
+    }
+    pt.J = J;
+    return pt;
+}
 
 bool finite(float v) { return std::isfinite(v); }
 
@@ -185,37 +208,33 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
 
     // Device facts; on a machine without a GPU the context can still be created (for
     // argument checks), sized for a 152-SM part, and every launch will fail.
-    int dev = -1, sms = 0;
+    int dev = -1, sms = 0, smem = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0 &&
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess) {
         c->device = dev;
         c->sms = sms;
+        c->smem_budget = smem;
     } else {
         cudaGetLastError();
         c->device = -1;
         c->sms = 152;
+        c->smem_budget = 232448;
     }
-    int occ = 0;
-    if (c->device >= 0)
-        for (int dt = 0; dt < 3; ++dt) occ = occ > occupancy_worker(W, dt) ? occ : occupancy_worker(W, dt);
-    if (occ <= 0) occ = 2;
-    occ = pow2_floor(occ);
-
-    Part pt{};
-    pt.NG = n / 256;
-    pt.CG = chunk / 256;
-    pt.nchunks = c->nchunks;
-    const int64_t want = (int64_t)c->sms * occ * kWarpsPerBlock;
-    pt.P = want < pt.NG ? want : pt.NG;
-    int64_t J = 1;
-    for (int64_t q = 0; q < pt.P; ++q) {
-        const int64_t g0 = q * pt.NG / pt.P, g1 = (q + 1) * pt.NG / pt.P;
-        const int64_t span = (g1 - 1) / pt.CG - g0 / pt.CG + 1;
-        if (span > J) J = span;
+    // worker: one block per SM, one warp per range
+    int64_t wpart = 0;
+    for (int dt = 0; dt < 3; ++dt) {
+        const WorkerConfig wc = worker_config(W, dt, c->smem_budget);
+        c->ptw[dt] = make_part(n, chunk, (int64_t)c->sms * wc.warps_per_block);
+        const int64_t need = (int64_t)W * c->ptw[dt].P * c->ptw[dt].J;
+        if (need > wpart) wpart = need;
     }
-    pt.J = J;
-    c->pt = pt;
-    c->lay = make_layout(n, W, c->nchunks, pt.P, pt.J);
+    // server: all resident blocks, a power of two per SM
+    int occ = c->device >= 0 ? occupancy_server(W) : 0;
+    occ = pow2_floor(occ > 0 ? occ : 2);
+    c->grid_s = c->sms * occ;
+    c->pts = make_part(n, chunk, (int64_t)c->grid_s * kWarpsPerBlock);
+    c->lay = make_layout(n, W, c->nchunks, wpart, c->pts.P * c->pts.J);
     *out = c;
     return OB_OK;
 }
@@ -346,14 +365,17 @@ int ob_compressed_step(ob_ctx* c, const void* grads, int dtype, float* x, float*
     wa.s_next = at<float>(ws, L.s_next);
     wa.part = at<double>(ws, L.wpart);
     wa.cnt = at<unsigned>(ws, L.wcnt);
-    wa.pt = c->pt;
+    wa.status = at<unsigned>(ws, L.status);
+    wa.pt = c->ptw[dtype];
     wa.n = c->n;
     wa.C = c->C;
     wa.b1 = c->b1;
     wa.c1 = 1.0f - c->b1;
-    const int occ_w = pow2_floor(occupancy_worker(c->W, dtype));
-    const int grid_w = c->sms * (occ_w > 0 ? occ_w : 1);
-    if (int r = launch(c, OB_K_WORKER, s, [&] { return launch_worker(c->W, dtype, wa, grid_w, s); })) return r;
+    const int grid_w = c->sms;
+    if (int r = launch(c, OB_K_WORKER, s, [&] {
+            return launch_worker(c->W, dtype, wa, grid_w, s, c->smem_budget);
+        }))
+        return r;
 
     ServerArgs sa{};
     sa.wbits = wa.wbits;
@@ -364,12 +386,10 @@ int ob_compressed_step(ob_ctx* c, const void* grads, int dtype, float* x, float*
     sa.t_next = at<float>(ws, L.t_next);
     sa.part = at<double>(ws, L.spart);
     sa.cnt = at<unsigned>(ws, L.scnt);
-    sa.pt = c->pt;
+    sa.pt = c->pts;
     sa.n = c->n;
     sa.C = c->C;
-    const int occ_s = pow2_floor(occupancy_server(c->W));
-    const int grid_s = c->sms * (occ_s > 0 ? occ_s : 1);
-    if (int r = launch(c, OB_K_SERVER, s, [&] { return launch_server(c->W, sa, grid_s, s); })) return r;
+    if (int r = launch(c, OB_K_SERVER, s, [&] { return launch_server(c->W, sa, c->grid_s, s); })) return r;
 
     UpdateArgs ua{};
     ua.sbits = sa.sbits;
@@ -381,8 +401,8 @@ int ob_compressed_step(ob_ctx* c, const void* grads, int dtype, float* x, float*
     ua.s_prev = at<float>(ws, L.s_prev);
     ua.s_next = wa.s_next;
     ua.t_prev = at<float>(ws, L.t_prev);
-    ua.NG = c->pt.NG;
-    ua.CG = c->pt.CG;
+    ua.NG = c->pts.NG;
+    ua.CG = c->pts.CG;
     ua.nscales_w = (int64_t)c->W * c->nchunks;
     ua.nchunks = c->nchunks;
     ua.lr = c->lr;
@@ -566,6 +586,19 @@ int ob_profile_read(ob_ctx* c, int kernel, double* total_ms, int64_t* launches)
 
 int64_t ob_launch_count(const ob_ctx* c) { return c ? c->launches : -1; }
 
+int ob_read_status(ob_ctx* c, const void* ws, unsigned* status, void* stream)
+{
+    if (!c || !status) return OB_EINVAL;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(status, at<unsigned>(const_cast<void*>(ws), c->lay.status), 4,
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return OB_OK;
+}
+
 const char* ob_strerror(int code)
 {
     switch (code) {
@@ -630,16 +663,18 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
         if (int r = check_ptr(p, 16)) return r;
     if (scale_prev == scale_out) return OB_EINVAL;
     // scratch: partial sums [W][P][J] doubles, then one counter per chunk
-    const size_t part_bytes = up((size_t)c->W * c->pt.P * c->pt.J * 8, kAlignWs);
-    const size_t cnt_bytes = (size_t)c->nchunks * 4;
-    if (part_bytes + cnt_bytes > (size_t)OB_NOALLOC_SCRATCH_BYTES) return OB_ESCRATCH;
+    const Part& pt = c->ptw[dtype];
+    const size_t part_bytes = up((size_t)c->W * pt.P * pt.J * 8, kAlignWs);
+    const size_t cnt_bytes = up((size_t)c->nchunks * 4, 16);
+    if (part_bytes + cnt_bytes + 16 > (size_t)OB_NOALLOC_SCRATCH_BYTES) return OB_ESCRATCH;
     if (int r = check_device(c)) return r;
     void* scratch = nullptr;
     if (int r = noalloc_scratch(c->device, &scratch)) return r;
     const cudaStream_t s = (cudaStream_t)stream;
     unsigned* cnt = at<unsigned>(scratch, part_bytes);
-    // the counters must start at zero; the partials are written before they are read
-    const cudaError_t e = cudaMemsetAsync(cnt, 0, cnt_bytes, s);
+    // the counters (and the status word after them) must start at zero; the partials are
+    // written before they are read
+    const cudaError_t e = cudaMemsetAsync(cnt, 0, cnt_bytes + 16, s);
     if (e != cudaSuccess) return cuda_fail(e);
 
     WorkerArgs wa{};
@@ -651,12 +686,12 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
     wa.s_next = scale_out;
     wa.part = at<double>(scratch, 0);
     wa.cnt = cnt;
-    wa.pt = c->pt;
+    wa.status = at<unsigned>(scratch, part_bytes + cnt_bytes);
+    wa.pt = pt;
     wa.n = c->n;
     wa.C = c->C;
     wa.b1 = c->b1;
     wa.c1 = 1.0f - c->b1;
-    const int occ_w = pow2_floor(occupancy_worker(c->W, dtype));
-    const int grid_w = c->sms * (occ_w > 0 ? occ_w : 1);
-    return launch(c, OB_K_WORKER, s, [&] { return launch_worker(c->W, dtype, wa, grid_w, s); });
+    const int grid_w = c->sms;
+    return launch(c, OB_K_WORKER, s, [&] { return launch_worker(c->W, dtype, wa, grid_w, s, c->smem_budget); });
 }

@@ -24,9 +24,19 @@ struct WorkerArgs {
     float* s_next;          // [W][nchunks] scales of this step (written by the last contributor)
     double* part;           // [W][P][J] partial sums of squares
     unsigned* cnt;          // [nchunks] arrival counters (zero between launches)
+    unsigned* status;       // status word (0 = fine; see ob_tma.cuh)
     Part pt;
     int64_t n, C;
     float b1, c1;
+    int stages;             // pipeline stages per warp (set by the launcher)
+};
+
+// Launch shape of the worker kernel for one (W, gradient type).
+struct WorkerConfig {
+    int warps_per_block;
+    int stages;
+    size_t smem_bytes;
+    uint32_t stage_bytes;
 };
 
 struct ServerArgs {
@@ -100,7 +110,8 @@ struct LocoArgs {
 
 // Launchers (return the launch status). `grid` blocks of kBlock threads.
 constexpr int kBlock = 256;
-cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaStream_t s, int smem_budget);
+WorkerConfig worker_config(int W, int dtype, int smem_budget);
 cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_warmup(int dtype, const WarmupArgs& a, int grid, cudaStream_t s);
@@ -110,8 +121,7 @@ cudaError_t launch_loco_absmax(int dtype, const LocoArgs& a, int grid, cudaStrea
 cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s);
 
-// Resident blocks per SM of the worker / server kernel for (W, dtype); 0 on error.
-int occupancy_worker(int W, int dtype);
+// Resident blocks per SM of the server kernel for W; 0 on error.
 int occupancy_server(int W);
 
 }  // namespace ob

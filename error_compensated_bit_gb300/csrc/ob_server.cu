@@ -13,18 +13,58 @@
 
 namespace ob {
 
+// (sum over w ascending of +-S_w) / W for one element, the definition itself. A
+// division by a power of two is exact, so it is done as a multiplication there.
+template <int W>
+__device__ __forceinline__ float average_of_signs(const float (&sw)[W], uint32_t pattern)
+{
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) sum = __fadd_rn(sum, signed_scale(sw[w], (pattern >> w) & 1u));
+    if ((W & (W - 1)) == 0) return __fmul_rn(sum, 1.0f / (float)W);
+    return __fdiv_rn(sum, (float)W);
+}
+
+// All elements of a chunk share the W scales, so the server average depends only on the
+// element's W sign bits: for W <= 8 a warp tabulates it for all 2^W sign patterns once per
+// chunk (each entry evaluated exactly as above) and looks it up per element.
+template <int W>
+__device__ __forceinline__ void build_average_table(float* tab, const float (&sw)[W], int lane)
+{
+    __syncwarp();                       // the previous chunk's table is no longer read
+    for (uint32_t e = lane; e < (1u << W); e += 32) tab[e] = average_of_signs<W>(sw, e);
+    __syncwarp();
+}
+
+// 8x8 bit-matrix transpose (three delta swaps, as in Hacker's Delight): in, byte r bit c
+// is entry (r, c); out, byte c bit r. With byte w = worker w's signs of this lane's 8
+// elements, output byte j is element j's sign pattern (bit w = worker w).
+__device__ __forceinline__ uint64_t transpose8x8(uint64_t x)
+{
+    uint64_t t;
+    t = (x ^ (x >> 7)) & 0x00AA00AA00AA00AAull;
+    x = x ^ t ^ (t << 7);
+    t = (x ^ (x >> 14)) & 0x0000CCCC0000CCCCull;
+    x = x ^ t ^ (t << 14);
+    t = (x ^ (x >> 28)) & 0x00000000F0F0F0F0ull;
+    x = x ^ t ^ (t << 28);
+    return x;
+}
+
 // a = (sum over w ascending of +-S_wk)/W;  e_s = yprev - T_prev*sign(yprev);  y = a + e_s;
 // bit = (y >= 0); ybuf = y; chunk sums of y^2 -> T_next.
 // Memory per element: W/8 (worker bits) + 4 + 4 (y) + 1/8 (server bits).
 template <int W>
 __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 {
+    constexpr bool kTable = W <= 8;
+    __shared__ float s_tab[kTable ? (kBlock / 32) << W : 1];
+    float* tab = s_tab + (kTable ? (threadIdx.x >> 5) << W : 0);
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const Part pt = a.pt;
     const int64_t words_per_row = a.n / 32;
-    const float fW = (float)W;
 
     for (int64_t q = warp; q < pt.P; q += nwarps) {
         const int64_t g0 = range_begin(pt, q);
@@ -37,6 +77,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 #pragma unroll
         for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
         float tp = __ldg(a.t_prev + k);
+        if (kTable) build_average_table<W>(tab, sw, lane);
         Sum2 acc[1] = {{0.0f, 0.0f}};
 
         for (int64_t gi = g0; gi < g1; ++gi) {
@@ -47,20 +88,32 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 #pragma unroll
                 for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
                 tp = __ldg(a.t_prev + k);
+                if (kTable) build_average_table<W>(tab, sw, lane);
             }
             uint32_t bytes[W];
 #pragma unroll
             for (int w = 0; w < W; ++w) bytes[w] = lane_byte(a.wbits + (int64_t)w * words_per_row, gi, lane);
+            uint64_t patterns = 0;
+            if (kTable) {
+#pragma unroll
+                for (int w = 0; w < W; ++w) patterns |= (uint64_t)bytes[w] << (8 * w);
+                patterns = transpose8x8(patterns);
+            }
             const int64_t e0 = gi * 256 + lane * 8;
             float yv[8];
             ld8_stream(a.ybuf + e0, yv);
             uint32_t byte = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                float sum = 0.0f;
+                float avg;
+                if (kTable) {
+                    avg = tab[(uint32_t)(patterns >> (8 * j)) & 0xffu];
+                } else {
+                    uint32_t pat = 0;
 #pragma unroll
-                for (int w = 0; w < W; ++w) sum = __fadd_rn(sum, signed_scale(sw[w], (bytes[w] >> j) & 1u));
-                const float avg = __fdiv_rn(sum, fW);
+                    for (int w = 0; w < W; ++w) pat |= ((bytes[w] >> j) & 1u) << w;
+                    avg = average_of_signs<W>(sw, pat);
+                }
                 const float es = __fsub_rn(yv[j], signed_scale(tp, yv[j] >= 0.0f));
                 const float y = __fadd_rn(avg, es);
                 yv[j] = y;

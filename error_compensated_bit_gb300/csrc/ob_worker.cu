@@ -17,21 +17,109 @@
 // Memory per element: W*(grad bytes + 4 read + 4 write + 1/8 bits) + 4 (m), all
 // coalesced 16-byte accesses with streaming cache hints; m is read once for all W.
 #include "ob_common.cuh"
+#include "ob_tma.cuh"
 
 namespace ob {
 
+// Shared-memory pipeline. A stage holds one 256-element group of all W gradient rows, all
+// W z rows and m, filled by 2W+1 bulk copies (TMA) issued by lane 0 and counted by one
+// mbarrier; each warp owns `stages` consecutive stages. Bytes in flight then scale with
+// shared memory (up to ~200 KB per SM) rather than with the registers that plain loads
+// need, which is what a streaming kernel needs to reach HBM bandwidth.
 template <int W, typename G>
-__global__ void __launch_bounds__(kBlock) k_worker(WorkerArgs a)
+struct WorkerStage {
+    static constexpr uint32_t kGradRow = 256 * sizeof(G);
+    static constexpr uint32_t kZRow = 256 * 4;
+    static constexpr uint32_t kBytes = W * kGradRow + W * kZRow + 256 * 4;
+    static constexpr uint32_t kZOff = W * kGradRow;
+    static constexpr uint32_t kMOff = W * kGradRow + W * kZRow;
+};
+
+constexpr uint32_t kBarBytes = 8 * 8 * 8;   // up to 8 warps x 8 stages of 8-byte mbarriers
+
+template <typename G>
+__device__ __forceinline__ void ld8_shared(const unsigned char* row, int lane, float (&v)[8]);
+
+template <>
+__device__ __forceinline__ void ld8_shared<float>(const unsigned char* row, int lane, float (&v)[8])
 {
+    const float4 a = reinterpret_cast<const float4*>(row)[2 * lane];
+    const float4 b = reinterpret_cast<const float4*>(row)[2 * lane + 1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <>
+__device__ __forceinline__ void ld8_shared<__half>(const unsigned char* row, int lane, float (&v)[8])
+{
+    const uint4 r = reinterpret_cast<const uint4*>(row)[lane];
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h;
+        memcpy(&h, &w[i], 4);
+        const float2 f = __half22float2(h);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+template <>
+__device__ __forceinline__ void ld8_shared<__nv_bfloat16>(const unsigned char* row, int lane, float (&v)[8])
+{
+    const uint4 r = reinterpret_cast<const uint4*>(row)[lane];
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+template <int W, typename G>
+__global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
+{
+    using St = WorkerStage<W, G>;
+    extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int S = a.stages;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const Part pt = a.pt;
     const int64_t words_per_row = a.n / 32;
+    const uint32_t bar0 = smem_u32(smem) + 8u * (uint32_t)(wib * S);
+    unsigned char* stage0 = smem + kBarBytes + (size_t)wib * S * St::kBytes;
+    const uint32_t st0 = smem_u32(stage0);
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bar0 + 8u * s, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    const uint64_t pol = policy_evict_first();
+    uint32_t phase = 0;   // bit s: parity of stage s's next completion
+
+    // lane 0: fill stage s with group gi
+    auto issue = [&](int s, int64_t gi) {
+        const uint32_t bar = bar0 + 8u * s;
+        const uint32_t dst = st0 + (uint32_t)s * St::kBytes;
+        const int64_t e0 = gi * 256;
+        mbar_arrive_expect(bar, St::kBytes);
+#pragma unroll
+        for (int w = 0; w < W; ++w)
+            bulk_load_hint(dst + w * St::kGradRow, static_cast<const G*>(a.g) + (int64_t)w * a.n + e0,
+                           St::kGradRow, bar, pol);
+#pragma unroll
+        for (int w = 0; w < W; ++w)
+            bulk_load_hint(dst + St::kZOff + w * St::kZRow, a.zbuf + (int64_t)w * a.n + e0, St::kZRow, bar, pol);
+        bulk_load(dst + St::kMOff, a.m + e0, 256 * 4, bar);
+    };
 
     for (int64_t q = warp; q < pt.P; q += nwarps) {
         const int64_t g0 = range_begin(pt, q);
         const int64_t g1 = range_begin(pt, q + 1);
+        const int64_t count = g1 - g0;
         int64_t k = g0 / pt.CG;
         const int64_t kfirst = k;
         int64_t kend = (k + 1) * pt.CG;
@@ -44,8 +132,11 @@ __global__ void __launch_bounds__(kBlock) k_worker(WorkerArgs a)
             acc[w].s = 0.0f;
             acc[w].e = 0.0f;
         }
+        if (lane == 0)
+            for (int i = 0; i < S && i < count; ++i) issue(i, g0 + i);
 
-        for (int64_t gi = g0; gi < g1; ++gi) {
+        for (int64_t i = 0; i < count; ++i) {
+            const int64_t gi = g0 + i;
             if (gi == kend) {
                 flush_chunk<W>(pt, q, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
                 ++k;
@@ -53,18 +144,30 @@ __global__ void __launch_bounds__(kBlock) k_worker(WorkerArgs a)
 #pragma unroll
                 for (int w = 0; w < W; ++w) sp[w] = __ldg(a.s_prev + (int64_t)w * pt.nchunks + k);
             }
+            const int s = (int)(i % S);
+            const bool landed = __all_sync(kFull, mbar_wait(bar0 + 8u * s, (phase >> s) & 1u));
+            if (!landed) {
+                // record the failure, let every copy still in flight land, and stop
+                if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+                for (int64_t t = i; t < count && t < i + S; ++t) {
+                    const int st = (int)(t % S);
+                    mbar_wait(bar0 + 8u * st, (phase >> st) & 1u);
+                }
+                return;
+            }
+            phase ^= 1u << s;
+            const unsigned char* stg = stage0 + (size_t)s * St::kBytes;
             const int64_t e0 = gi * 256 + lane * 8;
             float bm[8];
-            ld8_stream(a.m + e0, bm);
+            ld8_shared<float>(stg + St::kMOff, lane, bm);
 #pragma unroll
             for (int j = 0; j < 8; ++j) bm[j] = __fmul_rn(a.b1, bm[j]);
 
 #pragma unroll
             for (int w = 0; w < W; ++w) {
-                const int64_t row = (int64_t)w * a.n + e0;
                 float gv[8], zv[8];
-                Grad<G>::ld8(a.g, row, gv);
-                ld8_stream(a.zbuf + row, zv);
+                ld8_shared<G>(stg + w * St::kGradRow, lane, gv);
+                ld8_shared<float>(stg + St::kZOff + w * St::kZRow, lane, zv);
                 uint32_t byte = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -75,59 +178,95 @@ __global__ void __launch_bounds__(kBlock) k_worker(WorkerArgs a)
                     byte |= (z >= 0.0f ? 1u : 0u) << j;
                     sum2_add_sq(acc[w], z);
                 }
-                st8_stream(a.zbuf + row, zv);
+                st8_stream(a.zbuf + (int64_t)w * a.n + e0, zv);
                 const uint32_t word = quad_word(byte, lane);
                 if ((lane & 3) == 0) __stcs(a.wbits + (int64_t)w * words_per_row + gi * 8 + (lane >> 2), word);
             }
+            __syncwarp();                   // every lane is done with stage s
+            if (lane == 0 && i + S < count) issue(s, gi + S);
         }
         flush_chunk<W>(pt, q, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
     }
 }
 
-template <int W>
-static cudaError_t launch_w(int dtype, const WorkerArgs& a, int grid, cudaStream_t s)
+// Launch shape for (W, gradient type): warps per block and stages per warp chosen so that
+// the stages fill the shared memory of one block (one block per SM): at least two stages
+// per warp, up to eight warps, and as many stages as then fit (at most eight).
+template <int W, typename G>
+static WorkerConfig config_w(int smem_budget)
 {
-    if (dtype == 0) k_worker<W, float><<<grid, kBlock, 0, s>>>(a);
-    else if (dtype == 1) k_worker<W, __half><<<grid, kBlock, 0, s>>>(a);
-    else k_worker<W, __nv_bfloat16><<<grid, kBlock, 0, s>>>(a);
+    using St = WorkerStage<W, G>;
+    WorkerConfig c{};
+    const int usable = smem_budget - (int)kBarBytes;
+    int warps = usable / (2 * (int)St::kBytes);
+    warps = warps > 8 ? 8 : (warps < 1 ? 1 : warps);
+    int stages = usable / (warps * (int)St::kBytes);
+    stages = stages > 8 ? 8 : (stages < 2 ? 2 : stages);
+    c.warps_per_block = warps;
+    c.stages = stages;
+    c.smem_bytes = kBarBytes + (size_t)warps * stages * St::kBytes;
+    c.stage_bytes = St::kBytes;
+    return c;
+}
+
+template <int W, typename G>
+static cudaError_t launch_wg(const WorkerArgs& a, int grid, cudaStream_t s, int smem_budget)
+{
+    const WorkerConfig c = config_w<W, G>(smem_budget);
+    if ((int)c.smem_bytes > smem_budget) return cudaErrorInvalidConfiguration;
+    static bool attr_set = false;   // per instantiation; the budget does not change per process
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(k_worker<W, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)c.smem_bytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    WorkerArgs b = a;
+    b.stages = c.stages;
+    k_worker<W, G><<<grid, c.warps_per_block * 32, c.smem_bytes, s>>>(b);
     return cudaGetLastError();
 }
 
 template <int W>
-static int occ_w(int dtype)
+static cudaError_t launch_w(int dtype, const WorkerArgs& a, int grid, cudaStream_t s, int smem_budget)
 {
-    int blocks = 0;
-    cudaError_t e;
-    if (dtype == 0) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_worker<W, float>, kBlock, 0);
-    else if (dtype == 1) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_worker<W, __half>, kBlock, 0);
-    else e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_worker<W, __nv_bfloat16>, kBlock, 0);
-    return e == cudaSuccess ? blocks : 0;
+    if (dtype == 0) return launch_wg<W, float>(a, grid, s, smem_budget);
+    if (dtype == 1) return launch_wg<W, __half>(a, grid, s, smem_budget);
+    return launch_wg<W, __nv_bfloat16>(a, grid, s, smem_budget);
+}
+
+template <int W>
+static WorkerConfig cfg_w(int dtype, int smem_budget)
+{
+    if (dtype == 0) return config_w<W, float>(smem_budget);
+    if (dtype == 1) return config_w<W, __half>(smem_budget);
+    return config_w<W, __nv_bfloat16>(smem_budget);
 }
 
 #define OB_FOR_EACH_W(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(16)
 
-cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaStream_t s)
+cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaStream_t s, int smem_budget)
 {
     switch (W) {
 #define OB_CASE(w) \
     case w:        \
-        return launch_w<w>(dtype, a, grid, s);
+        return launch_w<w>(dtype, a, grid, s, smem_budget);
         OB_FOR_EACH_W(OB_CASE)
 #undef OB_CASE
     }
     return cudaErrorInvalidValue;
 }
 
-int occupancy_worker(int W, int dtype)
+WorkerConfig worker_config(int W, int dtype, int smem_budget)
 {
     switch (W) {
 #define OB_CASE(w) \
     case w:        \
-        return occ_w<w>(dtype);
+        return cfg_w<w>(dtype, smem_budget);
         OB_FOR_EACH_W(OB_CASE)
 #undef OB_CASE
     }
-    return 0;
+    return WorkerConfig{};
 }
 
 }  // namespace ob

@@ -50,6 +50,7 @@ SIGNATURES = {
     "ob_profile_read": (_int, [_vp, _int, ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(_i64)]),
     "ob_launch_count": (_i64, [_vp]),
+    "ob_read_status": (_int, [_vp, _vp, ctypes.POINTER(ctypes.c_uint), _vp]),
     "ob_strerror": (ctypes.c_char_p, [_int]),
     "ob_last_cuda_error": (_int, []),
     "ob_worker_compress_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -204,6 +205,12 @@ class Context:
 
     def launch_count(self):
         return int(_lib().ob_launch_count(self.h))
+
+    def read_status(self, ws, stream=None):
+        """Synchronize and return the workspace status word (0 = every kernel finished)."""
+        st = ctypes.c_uint()
+        _call("ob_read_status", self.h, _ptr(ws), ctypes.byref(st), _stream(stream))
+        return st.value
 
     def worker_compress_noalloc(self, grads, m, worker_err, scale_prev, wbits, scale_out,
                                 stream=None):

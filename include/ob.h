@@ -227,6 +227,15 @@ int ob_profile_read(ob_ctx *ctx, int kernel, double *total_ms, int64_t *launches
 /* Kernels this context has launched in total. */
 int64_t ob_launch_count(const ob_ctx *ctx);
 
+/*
+ * Synchronize the stream, then copy the workspace's status word to *status: 0 when every
+ * kernel finished normally; 1 when a kernel gave up waiting for a shared-memory pipeline
+ * stage (every such wait is bounded, about two seconds). A non-zero status means the
+ * step's outputs are not valid; re-initialise the workspace (ob_workspace_init) and the
+ * error buffers before continuing.
+ */
+int ob_read_status(ob_ctx *ctx, const void *ws, unsigned *status, void *stream);
+
 /* Text for a status code; the last CUDA error number seen by this thread. */
 const char *ob_strerror(int code);
 int ob_last_cuda_error(void);
