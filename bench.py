@@ -340,7 +340,7 @@ def gpu_arm(args, wl):
     b_step = n * bytes_per_elem(args.phase, W, s_g, masked)
     if args.phase == "compressed":
         k_bytes = n * worker_bytes_per_elem(W, s_g)
-        khash = kernel_source_hash(["ob_worker.cu", "ob_common.cuh"])
+        khash = kernel_source_hash(["ob_worker.cu", "ob_common.cuh", "ob_tma.cuh"])
     elif args.phase == "warmup":
         k_bytes = n * (W * s_g + 24.0)
         khash = kernel_source_hash(["ob_warmup.cu", "ob_common.cuh"])
