@@ -13,26 +13,24 @@
 
 namespace ob {
 
-// (sum over w ascending of +-S_w) / W for one element, the definition itself. A
-// division by a power of two is exact, so it is done as a multiplication there.
-template <int W>
-__device__ __forceinline__ float average_of_signs(const float (&sw)[W], uint32_t pattern)
-{
-    float sum = 0.0f;
-#pragma unroll
-    for (int w = 0; w < W; ++w) sum = __fadd_rn(sum, signed_scale(sw[w], (pattern >> w) & 1u));
-    if ((W & (W - 1)) == 0) return __fmul_rn(sum, 1.0f / (float)W);
-    return __fdiv_rn(sum, (float)W);
-}
-
 // All elements of a chunk share the W scales, so the server average depends only on the
-// element's W sign bits: for W <= 8 a warp tabulates it for all 2^W sign patterns once per
-// chunk (each entry evaluated exactly as above) and looks it up per element.
+// element's W sign bits. A warp tabulates, once per chunk, the running sum over the first
+// min(W, 8) workers for all their sign patterns -- each entry summed in the same order as
+// the definition, so it is exactly the float32 partial sum the definition reaches after
+// those workers. For W <= 8 the entry is already divided by W (the final average); for
+// W > 8 the element continues the sum over the remaining workers in order.
 template <int W>
 __device__ __forceinline__ void build_average_table(float* tab, const float (&sw)[W], int lane)
 {
+    constexpr int T = W < 8 ? W : 8;
     __syncwarp();                       // the previous chunk's table is no longer read
-    for (uint32_t e = lane; e < (1u << W); e += 32) tab[e] = average_of_signs<W>(sw, e);
+    for (uint32_t e = lane; e < (1u << T); e += 32) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < T; ++w) sum = __fadd_rn(sum, signed_scale(sw[w], (e >> w) & 1u));
+        if (W <= 8) sum = (W & (W - 1)) == 0 ? __fmul_rn(sum, 1.0f / (float)W) : __fdiv_rn(sum, (float)W);
+        tab[e] = sum;
+    }
     __syncwarp();
 }
 
@@ -57,9 +55,9 @@ __device__ __forceinline__ uint64_t transpose8x8(uint64_t x)
 template <int W>
 __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 {
-    constexpr bool kTable = W <= 8;
-    __shared__ float s_tab[kTable ? (kBlock / 32) << W : 1];
-    float* tab = s_tab + (kTable ? (threadIdx.x >> 5) << W : 0);
+    constexpr int T = W < 8 ? W : 8;     // workers covered by the table
+    __shared__ float s_tab[(kBlock / 32) << T];
+    float* tab = s_tab + ((threadIdx.x >> 5) << T);
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -77,7 +75,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 #pragma unroll
         for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
         float tp = __ldg(a.t_prev + k);
-        if (kTable) build_average_table<W>(tab, sw, lane);
+        build_average_table<W>(tab, sw, lane);
         Sum2 acc[1] = {{0.0f, 0.0f}};
 
         for (int64_t gi = g0; gi < g1; ++gi) {
@@ -88,16 +86,19 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 #pragma unroll
                 for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
                 tp = __ldg(a.t_prev + k);
-                if (kTable) build_average_table<W>(tab, sw, lane);
+                build_average_table<W>(tab, sw, lane);
             }
             uint32_t bytes[W];
 #pragma unroll
             for (int w = 0; w < W; ++w) bytes[w] = lane_byte(a.wbits + (int64_t)w * words_per_row, gi, lane);
-            uint64_t patterns = 0;
-            if (kTable) {
+            uint64_t lo = 0, hi = 0;
 #pragma unroll
-                for (int w = 0; w < W; ++w) patterns |= (uint64_t)bytes[w] << (8 * w);
-                patterns = transpose8x8(patterns);
+            for (int w = 0; w < T; ++w) lo |= (uint64_t)bytes[w] << (8 * w);
+            lo = transpose8x8(lo);
+            if (W > 8) {
+#pragma unroll
+                for (int w = 8; w < W; ++w) hi |= (uint64_t)bytes[w] << (8 * (w - 8));
+                hi = transpose8x8(hi);
             }
             const int64_t e0 = gi * 256 + lane * 8;
             float yv[8];
@@ -105,14 +106,12 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
             uint32_t byte = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                float avg;
-                if (kTable) {
-                    avg = tab[(uint32_t)(patterns >> (8 * j)) & 0xffu];
-                } else {
-                    uint32_t pat = 0;
+                float avg = tab[(uint32_t)(lo >> (8 * j)) & 0xffu];
+                if (W > 8) {
+                    const uint32_t pat = (uint32_t)(hi >> (8 * j)) & 0xffu;
 #pragma unroll
-                    for (int w = 0; w < W; ++w) pat |= ((bytes[w] >> j) & 1u) << w;
-                    avg = average_of_signs<W>(sw, pat);
+                    for (int w = 8; w < W; ++w) avg = __fadd_rn(avg, signed_scale(sw[w], (pat >> (w - 8)) & 1u));
+                    avg = (W & (W - 1)) == 0 ? __fmul_rn(avg, 1.0f / (float)W) : __fdiv_rn(avg, (float)W);
                 }
                 const float es = __fsub_rn(yv[j], signed_scale(tp, yv[j] >= 0.0f));
                 const float y = __fadd_rn(avg, es);

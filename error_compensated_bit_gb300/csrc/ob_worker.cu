@@ -21,18 +21,21 @@
 
 namespace ob {
 
-// Shared-memory pipeline. A stage holds one 256-element group of all W gradient rows, all
-// W z rows and m, filled by 2W+1 bulk copies (TMA) issued by lane 0 and counted by one
-// mbarrier; each warp owns `stages` consecutive stages. Bytes in flight then scale with
-// shared memory (up to ~200 KB per SM) rather than with the registers that plain loads
-// need, which is what a streaming kernel needs to reach HBM bandwidth.
+// Shared-memory pipeline. A stage holds one 256-element group of up to eight gradient
+// rows and the matching z rows (plus m in a group's first stage), filled by bulk copies
+// (TMA) issued by lane 0 and counted by one mbarrier; with W > 8 a group takes two stages.
+// Each warp owns `stages` consecutive stages. Bytes in flight then scale with shared
+// memory (up to ~200 KB per SM) rather than with the registers that plain loads need,
+// which is what a streaming kernel needs to reach HBM bandwidth.
 template <int W, typename G>
 struct WorkerStage {
+    static constexpr int kRows = W < 8 ? W : 8;                 // rows per stage
+    static constexpr int kBlocks = (W + kRows - 1) / kRows;     // stages per group
     static constexpr uint32_t kGradRow = 256 * sizeof(G);
     static constexpr uint32_t kZRow = 256 * 4;
-    static constexpr uint32_t kBytes = W * kGradRow + W * kZRow + 256 * 4;
-    static constexpr uint32_t kZOff = W * kGradRow;
-    static constexpr uint32_t kMOff = W * kGradRow + W * kZRow;
+    static constexpr uint32_t kZOff = kRows * kGradRow;
+    static constexpr uint32_t kMOff = kRows * (kGradRow + kZRow);
+    static constexpr uint32_t kBytes = kMOff + 256 * 4;
 };
 
 constexpr uint32_t kBarBytes = 8 * 8 * 8;   // up to 8 warps x 8 stages of 8-byte mbarriers
@@ -80,6 +83,8 @@ template <int W, typename G>
 __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
 {
     using St = WorkerStage<W, G>;
+    constexpr int R = St::kRows;
+    constexpr int NB = St::kBlocks;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
@@ -100,30 +105,31 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
     const uint64_t pol = policy_evict_first();
     uint32_t phase = 0;   // bit s: parity of stage s's next completion
 
-    // lane 0: fill stage s with group gi
-    auto issue = [&](int s, int64_t gi) {
-        const uint32_t bar = bar0 + 8u * s;
-        const uint32_t dst = st0 + (uint32_t)s * St::kBytes;
-        const int64_t e0 = gi * 256;
-        mbar_arrive_expect(bar, St::kBytes);
-#pragma unroll
-        for (int w = 0; w < W; ++w)
-            bulk_load_hint(dst + w * St::kGradRow, static_cast<const G*>(a.g) + (int64_t)w * a.n + e0,
-                           St::kGradRow, bar, pol);
-#pragma unroll
-        for (int w = 0; w < W; ++w)
-            bulk_load_hint(dst + St::kZOff + w * St::kZRow, a.zbuf + (int64_t)w * a.n + e0, St::kZRow, bar, pol);
-        bulk_load(dst + St::kMOff, a.m + e0, 256 * 4, bar);
-    };
-
     for (int64_t q = warp; q < pt.P; q += nwarps) {
         const int64_t g0 = range_begin(pt, q);
         const int64_t g1 = range_begin(pt, q + 1);
         const int64_t count = g1 - g0;
+        const int64_t items = count * NB;   // (group, row block) pairs, in order
+
+        // lane 0: fill stage s with item `it` of this range
+        auto issue = [&](int s, int64_t it) {
+            const uint32_t bar = bar0 + 8u * s;
+            const uint32_t dst = st0 + (uint32_t)s * St::kBytes;
+            const int64_t e0 = (g0 + it / NB) * 256;
+            const int b = (int)(it % NB);
+            const int rows = (W - b * R) < R ? (W - b * R) : R;
+            mbar_arrive_expect(bar, (uint32_t)rows * (St::kGradRow + St::kZRow) + (b == 0 ? 256u * 4u : 0u));
+            for (int r = 0; r < rows; ++r) {
+                const int64_t row = (int64_t)(b * R + r) * a.n + e0;
+                bulk_load_hint(dst + r * St::kGradRow, static_cast<const G*>(a.g) + row, St::kGradRow, bar, pol);
+                bulk_load_hint(dst + St::kZOff + r * St::kZRow, a.zbuf + row, St::kZRow, bar, pol);
+            }
+            if (b == 0) bulk_load(dst + St::kMOff, a.m + e0, 256 * 4, bar);
+        };
+
         int64_t k = g0 / pt.CG;
         const int64_t kfirst = k;
         int64_t kend = (k + 1) * pt.CG;
-
         float sp[W];
         Sum2 acc[W];
 #pragma unroll
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
             acc[w].e = 0.0f;
         }
         if (lane == 0)
-            for (int i = 0; i < S && i < count; ++i) issue(i, g0 + i);
+            for (int64_t it = 0; it < S && it < items; ++it) issue((int)it, it);
 
         for (int64_t i = 0; i < count; ++i) {
             const int64_t gi = g0 + i;
@@ -144,46 +150,54 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
 #pragma unroll
                 for (int w = 0; w < W; ++w) sp[w] = __ldg(a.s_prev + (int64_t)w * pt.nchunks + k);
             }
-            const int s = (int)(i % S);
-            const bool landed = __all_sync(kFull, mbar_wait(bar0 + 8u * s, (phase >> s) & 1u));
-            if (!landed) {
-                // record the failure, let every copy still in flight land, and stop
-                if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
-                for (int64_t t = i; t < count && t < i + S; ++t) {
-                    const int st = (int)(t % S);
-                    mbar_wait(bar0 + 8u * st, (phase >> st) & 1u);
-                }
-                return;
-            }
-            phase ^= 1u << s;
-            const unsigned char* stg = stage0 + (size_t)s * St::kBytes;
             const int64_t e0 = gi * 256 + lane * 8;
             float bm[8];
-            ld8_shared<float>(stg + St::kMOff, lane, bm);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) bm[j] = __fmul_rn(a.b1, bm[j]);
-
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                float gv[8], zv[8];
-                ld8_shared<G>(stg + w * St::kGradRow, lane, gv);
-                ld8_shared<float>(stg + St::kZOff + w * St::kZRow, lane, zv);
-                uint32_t byte = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float e = __fsub_rn(zv[j], signed_scale(sp[w], zv[j] >= 0.0f));
-                    const float p = __fadd_rn(bm[j], __fmul_rn(a.c1, gv[j]));
-                    const float z = __fadd_rn(p, e);
-                    zv[j] = z;
-                    byte |= (z >= 0.0f ? 1u : 0u) << j;
-                    sum2_add_sq(acc[w], z);
+            for (int b = 0; b < NB; ++b) {
+                const int64_t it = i * NB + b;
+                const int s = (int)(it % S);
+                const bool landed = __all_sync(kFull, mbar_wait(bar0 + 8u * s, (phase >> s) & 1u));
+                if (!landed) {
+                    // record the failure, let every copy still in flight land, and stop
+                    if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+                    for (int64_t t = it; t < items && t < it + S; ++t) {
+                        const int st = (int)(t % S);
+                        mbar_wait(bar0 + 8u * st, (phase >> st) & 1u);
+                    }
+                    return;
                 }
-                st8_stream(a.zbuf + (int64_t)w * a.n + e0, zv);
-                const uint32_t word = quad_word(byte, lane);
-                if ((lane & 3) == 0) __stcs(a.wbits + (int64_t)w * words_per_row + gi * 8 + (lane >> 2), word);
+                phase ^= 1u << s;
+                const unsigned char* stg = stage0 + (size_t)s * St::kBytes;
+                if (b == 0) {
+                    ld8_shared<float>(stg + St::kMOff, lane, bm);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) bm[j] = __fmul_rn(a.b1, bm[j]);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int w = b * R + r;
+                    if (w < W) {
+                        float gv[8], zv[8];
+                        ld8_shared<G>(stg + r * St::kGradRow, lane, gv);
+                        ld8_shared<float>(stg + St::kZOff + r * St::kZRow, lane, zv);
+                        uint32_t byte = 0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float e = __fsub_rn(zv[j], signed_scale(sp[w], zv[j] >= 0.0f));
+                            const float p = __fadd_rn(bm[j], __fmul_rn(a.c1, gv[j]));
+                            const float z = __fadd_rn(p, e);
+                            zv[j] = z;
+                            byte |= (z >= 0.0f ? 1u : 0u) << j;
+                            sum2_add_sq(acc[w], z);
+                        }
+                        st8_stream(a.zbuf + (int64_t)w * a.n + e0, zv);
+                        const uint32_t word = quad_word(byte, lane);
+                        if ((lane & 3) == 0) __stcs(a.wbits + (int64_t)w * words_per_row + gi * 8 + (lane >> 2), word);
+                    }
+                }
+                __syncwarp();               // every lane is done with stage s
+                if (lane == 0 && it + S < items) issue(s, it + S);
             }
-            __syncwarp();                   // every lane is done with stage s
-            if (lane == 0 && i + S < count) issue(s, gi + S);
         }
         flush_chunk<W>(pt, q, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
     }
