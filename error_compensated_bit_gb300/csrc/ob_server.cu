@@ -133,31 +133,48 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 // every kernel that reads the previous slots (worker, server) has finished by now.
 __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
 {
+    constexpr int U = 4;   // groups per warp iteration: all their loads are in flight together
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const bool masked = a.maskbits != nullptr;
 
-    for (int64_t gi = warp; gi < a.NG; gi += nwarps) {
-        const float T = __ldg(a.t_next + gi / a.CG);
-        const uint32_t sb = lane_byte(a.sbits, gi, lane);
-        const uint32_t mb = masked ? lane_byte(a.maskbits, gi, lane) : 0xffu;
-        const int64_t e0 = gi * 256 + lane * 8;
-        float vv[8], xv[8], mv[8];
-        ld8_stream(a.v + e0, vv);
-        ld8_stream(a.x + e0, xv);
+    for (int64_t gb = warp * U; gb < a.NG; gb += nwarps * U) {
+        float vv[U][8], xv[U][8];
+        uint32_t sb[U], mb[U];
+        float T[U];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float mi = signed_scale(T, (sb >> j) & 1u);
-            if (masked) mi = __fmul_rn(mi, ((mb >> j) & 1u) ? 1.0f : 0.0f);
-            mv[j] = mi;
-            const float denom = __fadd_rn(__fsqrt_rn(vv[j]), a.eps);
-            float u = __fdiv_rn(mi, denom);
-            if (a.wd != 0.0f) u = __fadd_rn(u, __fmul_rn(a.wd, xv[j]));
-            xv[j] = __fsub_rn(xv[j], __fmul_rn(a.lr, u));
+        for (int u = 0; u < U; ++u) {
+            const int64_t gi = gb + u;
+            if (gi < a.NG) {
+                const int64_t e0 = gi * 256 + lane * 8;
+                T[u] = __ldg(a.t_next + gi / a.CG);
+                sb[u] = lane_byte(a.sbits, gi, lane);
+                mb[u] = masked ? lane_byte(a.maskbits, gi, lane) : 0xffu;
+                ld8_stream(a.v + e0, vv[u]);
+                ld8_stream(a.x + e0, xv[u]);
+            }
         }
-        st8_stream(a.m + e0, mv);
-        st8_stream(a.x + e0, xv);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t gi = gb + u;
+            if (gi < a.NG) {
+                const int64_t e0 = gi * 256 + lane * 8;
+                float mv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float mi = signed_scale(T[u], (sb[u] >> j) & 1u);
+                    if (masked) mi = __fmul_rn(mi, ((mb[u] >> j) & 1u) ? 1.0f : 0.0f);
+                    mv[j] = mi;
+                    const float denom = __fadd_rn(__fsqrt_rn(vv[u][j]), a.eps);
+                    float uu = __fdiv_rn(mi, denom);
+                    if (a.wd != 0.0f) uu = __fadd_rn(uu, __fmul_rn(a.wd, xv[u][j]));
+                    xv[u][j] = __fsub_rn(xv[u][j], __fmul_rn(a.lr, uu));
+                }
+                st8_stream(a.m + e0, mv);
+                st8_stream(a.x + e0, xv[u]);
+            }
+        }
     }
 
     if (blockIdx.x == 0) {
