@@ -52,6 +52,11 @@ struct ob_ctx {
     std::vector<cudaEvent_t> spare;
     double prof_ms[OB_K_COUNT] = {};
     int64_t prof_n[OB_K_COUNT] = {};
+    // host-gradient path: a copy stream, an event for "copy landed", and per device
+    // gradient buffer an event recorded after the last worker pass that read it
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t copied = nullptr;
+    std::vector<std::pair<const void*, cudaEvent_t>> buffer_read;
 };
 
 namespace {
@@ -247,6 +252,9 @@ void ob_destroy(ob_ctx* c)
         cudaEventDestroy(r.b);
     }
     for (auto e : c->spare) cudaEventDestroy(e);
+    for (auto& b : c->buffer_read) cudaEventDestroy(b.second);
+    if (c->copied) cudaEventDestroy(c->copied);
+    if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
     delete c;
 }
 
@@ -343,8 +351,19 @@ int ob_warmup_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, 
     return OB_OK;
 }
 
+static int compressed_step_impl(ob_ctx* c, const void* grads, int dtype, float* x, float* m,
+                                const float* v, float* worker_err, float* server_err, void* ws,
+                                void* stream, cudaEvent_t after_worker);
+
 int ob_compressed_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, const float* v,
                        float* worker_err, float* server_err, void* ws, void* stream)
+{
+    return compressed_step_impl(c, grads, dtype, x, m, v, worker_err, server_err, ws, stream, nullptr);
+}
+
+static int compressed_step_impl(ob_ctx* c, const void* grads, int dtype, float* x, float* m,
+                                const float* v, float* worker_err, float* server_err, void* ws,
+                                void* stream, cudaEvent_t after_worker)
 {
     if (!c) return OB_EINVAL;
     if (int r = check_grads(c, grads, dtype)) return r;
@@ -376,6 +395,10 @@ int ob_compressed_step(ob_ctx* c, const void* grads, int dtype, float* x, float*
             return launch_worker(c->W, dtype, wa, grid_w, s, c->smem_budget);
         }))
         return r;
+    if (after_worker) {
+        const cudaError_t e = cudaEventRecord(after_worker, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
 
     ServerArgs sa{};
     sa.wbits = wa.wbits;
@@ -426,9 +449,34 @@ int ob_compressed_step_host(ob_ctx* c, const void* grads_host, void* grads_dev, 
     if (int r = check_device(c)) return r;
     const cudaStream_t s = (cudaStream_t)stream;
     const size_t gbytes = (size_t)c->W * (size_t)c->n * grad_bytes(dtype);
-    cudaError_t e = cudaMemcpyAsync(grads_dev, grads_host, gbytes, cudaMemcpyHostToDevice, s);
+    cudaError_t e = cudaSuccess;
+    if (!c->copy_stream) {
+        e = cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->copied, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    // the event that marks the last worker pass reading this device buffer
+    cudaEvent_t read_done = nullptr;
+    for (auto& b : c->buffer_read)
+        if (b.first == grads_dev) read_done = b.second;
+    if (!read_done) {
+        if (c->buffer_read.size() >= 8) {           // forget the oldest buffer
+            cudaEventSynchronize(c->buffer_read.front().second);
+            cudaEventDestroy(c->buffer_read.front().second);
+            c->buffer_read.erase(c->buffer_read.begin());
+        }
+        e = cudaEventCreateWithFlags(&read_done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+        c->buffer_read.emplace_back(grads_dev, read_done);
+    }
+    // copy on the copy stream once the buffer is free; the step waits for the copy
+    e = cudaStreamWaitEvent(c->copy_stream, read_done, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(grads_dev, grads_host, gbytes, cudaMemcpyHostToDevice, c->copy_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(c->copied, c->copy_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->copied, 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (int r = ob_compressed_step(c, grads_dev, dtype, x, m, v, worker_err, server_err, ws, stream)) return r;
+    if (int r = compressed_step_impl(c, grads_dev, dtype, x, m, v, worker_err, server_err, ws, stream, read_done))
+        return r;
     e = cudaMemcpyAsync(sbits_host, at<uint32_t>(ws, c->lay.sbits), (size_t)c->n / 8, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaMemcpyAsync(sscale_host, at<float>(ws, c->lay.t_next), (size_t)c->nchunks * 4,

@@ -165,11 +165,15 @@ int ob_compressed_step(ob_ctx *ctx, const void *grads, int dtype, float *x, floa
 
 /*
  * The same step with the gradients in HOST memory: copies grads_host ([W][n] in dtype,
- * preferably pinned) into the caller's device buffer grads_dev, runs the step, and
+ * pinned for full speed) into the caller's device buffer grads_dev, runs the step, and
  * copies the step's compressed result -- the server's packed signs (n/32 words) and
  * scales (n/chunk floats), i.e. what every worker receives -- into sbits_host and
- * sscale_host. All on the stream; the host buffers must stay valid until the stream
- * reaches the copies.
+ * sscale_host. The host-to-device copy runs on a stream the context owns: it waits only
+ * until no earlier worker pass of this context still reads grads_dev, and `stream` waits
+ * for the copy before the step's kernels. So a caller that alternates two device
+ * buffers between consecutive calls overlaps the next step's gradient copy with this
+ * step's kernels. The copies back run on `stream`. The host buffers must stay valid
+ * until `stream` has passed this call's work.
  */
 int ob_compressed_step_host(ob_ctx *ctx, const void *grads_host, void *grads_dev, int dtype,
                             float *x, float *m, const float *v, float *worker_err,

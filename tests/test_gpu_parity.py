@@ -270,3 +270,30 @@ def test_stream_ordering():
     ref.step(g)
     torch.cuda.synchronize()
     assert torch.equal(opt.x, ref.x) and torch.equal(opt.m, ref.m)
+
+
+def test_host_buffer_entry_point_matches_device_path():
+    """ob_compressed_step_host (host gradients in, compressed message out, alternating
+    device buffers so copies overlap earlier steps) computes exactly the device path."""
+    from error_compensated_bit_gb300 import ob
+    rng = np.random.default_rng(61)
+    W, n = 4, 4 * 256 * 300
+    C = n // W
+    st = random_state(rng, n, W, C)
+    a, b = GpuRun(st.copy()), GpuRun(st.copy())
+    grads = [torch.from_numpy(_grads(rng, W, n, "f16")) for _ in range(3)]
+    hosts = [g.pin_memory() for g in grads]
+    dev_bufs = [torch.empty(W, n, dtype=torch.float16, device="cuda") for _ in range(2)]
+    sb_host = torch.empty(n // 32, dtype=torch.int32).pin_memory()
+    ss_host = torch.empty(n // C, dtype=torch.float32).pin_memory()
+    for t in range(3):
+        a.compressed_step(grads[t].cuda())
+        b.ctx.compressed_step_host(hosts[t], dev_bufs[t % 2], b.x, b.m, b.v, b.ew, b.es, b.ws,
+                                   sb_host, ss_host)
+        torch.cuda.synchronize()
+        sa, sb_ = a.snapshot(), b.snapshot()
+        for k in ("wbits", "wscale", "sbits", "sscale", "x", "m", "z", "y"):
+            assert np.array_equal(np.asarray(sa[k]).view(np.uint8), np.asarray(sb_[k]).view(np.uint8)), (t, k)
+        assert np.array_equal(sb_host.numpy().view(np.uint32), sb_["sbits"])
+        assert np.array_equal(ss_host.numpy(), sb_["sscale"])
+    assert b.ctx.read_status(b.ws) == 0
