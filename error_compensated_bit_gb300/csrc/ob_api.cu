@@ -44,6 +44,7 @@ struct ob_ctx {
     Part ptw[3]{};              // worker partition per gradient type (one warp per range)
     Part pts{};                 // server partition
     int grid_s = 0;
+    int grid_u = 0;             // update kernel: one resident wave
     Layout lay{};
     bool has_mask = false;
     int64_t launches = 0;
@@ -226,12 +227,12 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
         c->sms = 152;
         c->smem_budget = 232448;
     }
-    // worker: one block per SM, one warp per range
+    // worker: one block per SM, one range per block
     int64_t wpart = 0;
     for (int dt = 0; dt < 3; ++dt) {
         const WorkerConfig wc = worker_config(W, dt, c->smem_budget);
-        c->ptw[dt] = make_part(n, chunk, (int64_t)c->sms * wc.warps_per_block);
-        const int64_t need = (int64_t)W * c->ptw[dt].P * c->ptw[dt].J;
+        c->ptw[dt] = make_part(n, chunk, (int64_t)c->sms);      // one range per block
+        const int64_t need = (int64_t)W * c->ptw[dt].P * wc.warps_per_block * c->ptw[dt].J;
         if (need > wpart) wpart = need;
     }
     // server: all resident blocks, a power of two per SM
@@ -239,6 +240,8 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
     occ = pow2_floor(occ > 0 ? occ : 2);
     c->grid_s = c->sms * occ;
     c->pts = make_part(n, chunk, (int64_t)c->grid_s * kWarpsPerBlock);
+    const int occ_u = c->device >= 0 ? occupancy_update() : 0;
+    c->grid_u = c->sms * (occ_u > 0 ? occ_u : 2);
     c->lay = make_layout(n, W, c->nchunks, wpart, c->pts.P * c->pts.J);
     *out = c;
     return OB_OK;
@@ -431,7 +434,7 @@ static int compressed_step_impl(ob_ctx* c, const void* grads, int dtype, float* 
     ua.lr = c->lr;
     ua.eps = c->eps;
     ua.wd = c->wd;
-    if (int r = launch(c, OB_K_UPDATE, s, [&] { return launch_update(ua, stream_grid(c), s); })) return r;
+    if (int r = launch(c, OB_K_UPDATE, s, [&] { return launch_update(ua, c->grid_u, s); })) return r;
     c->step += 1;
     return OB_OK;
 }
@@ -712,7 +715,8 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
     if (scale_prev == scale_out) return OB_EINVAL;
     // scratch: partial sums [W][P][J] doubles, then one counter per chunk
     const Part& pt = c->ptw[dtype];
-    const size_t part_bytes = up((size_t)c->W * pt.P * pt.J * 8, kAlignWs);
+    const int wpb = worker_config(c->W, dtype, c->smem_budget).warps_per_block;
+    const size_t part_bytes = up((size_t)c->W * pt.P * wpb * pt.J * 8, kAlignWs);
     const size_t cnt_bytes = up((size_t)c->nchunks * 4, 16);
     if (part_bytes + cnt_bytes + 16 > (size_t)OB_NOALLOC_SCRATCH_BYTES) return OB_ESCRATCH;
     if (int r = check_device(c)) return r;

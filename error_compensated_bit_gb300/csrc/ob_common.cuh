@@ -1,11 +1,12 @@
 // Device helpers shared by the compression-stage kernels (sm_103a).
 //
-// Work decomposition used by every streaming kernel here: the flat buffer is cut into
+// Work decomposition used by the streaming kernels here: the flat buffer is cut into
 // groups of 256 elements (one warp iteration: 8 consecutive elements per lane, i.e. two
 // 16-byte loads of float32 or one 16-byte load of a 16-bit gradient), and the groups
-// into P contiguous ranges of (nearly) equal length, one warp per range. A 256-element
-// group never straddles a chunk (chunk % 256 == 0), so a warp can accumulate a chunk's
-// sum of squares in registers and flush it when its range crosses a chunk boundary.
+// into P contiguous ranges of (nearly) equal length, each worked by one warp (server) or
+// by one block whose warps take its groups in turn (worker). A 256-element group never
+// straddles a chunk (chunk % 256 == 0), so a warp can accumulate a chunk's sum of squares
+// in registers and flush it when it moves to a later chunk.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -176,21 +177,24 @@ static __device__ __noinline__ double chunk_sumsq_exact(const float* row, int64_
 }
 
 // Flush this warp's sums of squares for chunk k (rows 0..R-1), and, if this warp is
-// the last contributor of chunk k, combine all contributors' partials in ascending
-// range order and write the chunk's RMS scales. No waiting: the last arrival does the
-// work; the counter is reset for the next launch. `rows` is the buffer the squares
-// came from (row r at rows + r*row_stride), read only on the degenerate slow path.
+// the last contributor of chunk k, combine all contributors' partials in a fixed order
+// and write the chunk's RMS scales. No waiting: the last arrival does the work; the
+// counter is reset for the next launch. A range q is worked by `wpr` warps (warp `wir`
+// of them here), each of which flushes one partial -- possibly zero -- for every chunk
+// the range touches, so chunk k has (ranges touching it) * wpr contributors, combined
+// range by range, warp by warp. `rows` is the buffer the squares came from (row r at
+// rows + r*row_stride), read only on the degenerate slow path.
 template <int R>
-__device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int64_t k, int64_t kfirst,
-                                            Sum2 (&acc)[R], double* part, unsigned* cnt,
-                                            float* scale_out, int64_t C, const float* rows,
-                                            int64_t row_stride, int lane)
+__device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, int wir, int64_t k,
+                                            int64_t kfirst, Sum2 (&acc)[R], double* part,
+                                            unsigned* cnt, float* scale_out, int64_t C,
+                                            const float* rows, int64_t row_stride, int lane)
 {
     const int64_t j = k - kfirst;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
-        if (lane == 0) part[((int64_t)r * pt.P + q) * pt.J + j] = d;
+        if (lane == 0) part[(((int64_t)r * pt.P + q) * wpr + wir) * pt.J + j] = d;
         acc[r].s = 0.0f;
         acc[r].e = 0.0f;
     }
@@ -200,18 +204,20 @@ __device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int64_t k
         int64_t lo, hi;
         chunk_contributors(pt, k, lo, hi);
         const unsigned prev = atomicAdd(cnt + k, 1u);
-        last = (prev == (unsigned)(hi - lo)) ? 1u : 0u;
+        last = (prev == (unsigned)((hi - lo + 1) * wpr - 1)) ? 1u : 0u;
     }
     last = __shfl_sync(kFull, last, 0);
     if (!last) return;
     __threadfence();
     int64_t lo, hi;
     chunk_contributors(pt, k, lo, hi);
+    const int64_t total = (hi - lo + 1) * wpr;
     for (int r = 0; r < R; ++r) {
         double sum = 0.0;
-        for (int64_t qq = lo + lane; qq <= hi; qq += 32) {
+        for (int64_t t = lane; t < total; t += 32) {
+            const int64_t qq = lo + t / wpr;
             const int64_t jj = k - range_begin(pt, qq) / pt.CG;
-            sum += __ldcg(part + ((int64_t)r * pt.P + qq) * pt.J + jj);
+            sum += __ldcg(part + (((int64_t)r * pt.P + qq) * wpr + t % wpr) * pt.J + jj);
         }
         sum = warp_sum(sum);
         if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);

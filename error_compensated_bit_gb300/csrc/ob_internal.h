@@ -22,7 +22,7 @@ struct WorkerArgs {
     uint32_t* wbits;        // [W][n/32]
     const float* s_prev;    // [W][nchunks] scales of the previous step
     float* s_next;          // [W][nchunks] scales of this step (written by the last contributor)
-    double* part;           // [W][P][J] partial sums of squares
+    double* part;           // [W][P][warps per block][J] partial sums of squares
     unsigned* cnt;          // [nchunks] arrival counters (zero between launches)
     unsigned* status;       // status word (0 = fine; see ob_tma.cuh)
     Part pt;
@@ -121,7 +121,8 @@ cudaError_t launch_loco_absmax(int dtype, const LocoArgs& a, int grid, cudaStrea
 cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s);
 
-// Resident blocks per SM of the server kernel for W; 0 on error.
+// Resident blocks per SM of the server kernel for W / of the update kernel; 0 on error.
 int occupancy_server(int W);
+int occupancy_update();
 
 }  // namespace ob

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 
         for (int64_t gi = g0; gi < g1; ++gi) {
             if (gi == kend) {
-                flush_chunk<1>(pt, q, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+                flush_chunk<1>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
                 ++k;
                 kend += pt.CG;
 #pragma unroll
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
             const uint32_t word = quad_word(byte, lane);
             if ((lane & 3) == 0) __stcs(a.sbits + gi * 8 + (lane >> 2), word);
         }
-        flush_chunk<1>(pt, q, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+        flush_chunk<1>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
 }
 
@@ -138,15 +138,17 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const bool masked = a.maskbits != nullptr;
+    // one contiguous, balanced range of groups per warp (the grid is one resident wave)
+    const int64_t g_end = (warp + 1) * a.NG / nwarps;
 
-    for (int64_t gb = warp * U; gb < a.NG; gb += nwarps * U) {
+    for (int64_t gb = warp * a.NG / nwarps; gb < g_end; gb += U) {
         float vv[U][8], xv[U][8];
         uint32_t sb[U], mb[U];
         float T[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t gi = gb + u;
-            if (gi < a.NG) {
+            if (gi < g_end) {
                 const int64_t e0 = gi * 256 + lane * 8;
                 T[u] = __ldg(a.t_next + gi / a.CG);
                 sb[u] = lane_byte(a.sbits, gi, lane);
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t gi = gb + u;
-            if (gi < a.NG) {
+            if (gi < g_end) {
                 const int64_t e0 = gi * 256 + lane * 8;
                 float mv[8];
 #pragma unroll
@@ -258,6 +260,12 @@ cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s)
 {
     k_update<<<grid, kBlock, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+int occupancy_update()
+{
+    int blocks = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_update, kBlock, 0) == cudaSuccess ? blocks : 0;
 }
 
 cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s)

@@ -21,15 +21,16 @@
 
 namespace ob {
 
-// Shared-memory pipeline. A stage holds one 256-element group of up to eight gradient
+// Shared-memory pipeline. A stage holds one 256-element group of up to four gradient
 // rows and the matching z rows (plus m in a group's first stage), filled by bulk copies
-// (TMA) issued by lane 0 and counted by one mbarrier; with W > 8 a group takes two stages.
+// (TMA) issued by lane 0 and counted by one mbarrier; with W > 4 a group takes several
+// stages. Small stages let up to 16 warps share one SM's shared memory.
 // Each warp owns `stages` consecutive stages. Bytes in flight then scale with shared
 // memory (up to ~200 KB per SM) rather than with the registers that plain loads need,
 // which is what a streaming kernel needs to reach HBM bandwidth.
 template <int W, typename G>
 struct WorkerStage {
-    static constexpr int kRows = W < 8 ? W : 8;                 // rows per stage
+    static constexpr int kRows = W < 4 ? W : 4;                 // rows per stage
     static constexpr int kBlocks = (W + kRows - 1) / kRows;     // stages per group
     static constexpr uint32_t kGradRow = 256 * sizeof(G);
     static constexpr uint32_t kZRow = 256 * 4;
@@ -38,7 +39,9 @@ struct WorkerStage {
     static constexpr uint32_t kBytes = kMOff + 256 * 4;
 };
 
-constexpr uint32_t kBarBytes = 8 * 8 * 8;   // up to 8 warps x 8 stages of 8-byte mbarriers
+constexpr int kMaxWarps = 16;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kBarBytes = 8 * kMaxWarps * kMaxStages;   // 8-byte mbarriers
 
 template <typename G>
 __device__ __forceinline__ void ld8_shared(const unsigned char* row, int lane, float (&v)[8]);
@@ -80,7 +83,7 @@ __device__ __forceinline__ void ld8_shared<__nv_bfloat16>(const unsigned char* r
 }
 
 template <int W, typename G>
-__global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
 {
     using St = WorkerStage<W, G>;
     constexpr int R = St::kRows;
@@ -88,9 +91,8 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
+    const int wpb = (int)(blockDim.x >> 5);
     const int S = a.stages;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const Part pt = a.pt;
     const int64_t words_per_row = a.n / 32;
     const uint32_t bar0 = smem_u32(smem) + 8u * (uint32_t)(wib * S);
@@ -105,17 +107,21 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
     const uint64_t pol = policy_evict_first();
     uint32_t phase = 0;   // bit s: parity of stage s's next completion
 
-    for (int64_t q = warp; q < pt.P; q += nwarps) {
+    // Each block works one contiguous range of groups; its warps take the range's groups
+    // in turn (warp wib: groups g0 + wib, g0 + wib + wpb, ...), so the warps of a block
+    // stream neighbouring rows together.
+    for (int64_t q = blockIdx.x; q < pt.P; q += gridDim.x) {
         const int64_t g0 = range_begin(pt, q);
         const int64_t g1 = range_begin(pt, q + 1);
-        const int64_t count = g1 - g0;
+        const int64_t count = g1 - g0 > wib ? (g1 - g0 - wib + wpb - 1) / wpb : 0;
         const int64_t items = count * NB;   // (group, row block) pairs, in order
+        const int64_t klast = (g1 - 1) / pt.CG;
 
         // lane 0: fill stage s with item `it` of this range
         auto issue = [&](int s, int64_t it) {
             const uint32_t bar = bar0 + 8u * s;
             const uint32_t dst = st0 + (uint32_t)s * St::kBytes;
-            const int64_t e0 = (g0 + it / NB) * 256;
+            const int64_t e0 = (g0 + wib + (it / NB) * wpb) * 256;
             const int b = (int)(it % NB);
             const int rows = (W - b * R) < R ? (W - b * R) : R;
             mbar_arrive_expect(bar, (uint32_t)rows * (St::kGradRow + St::kZRow) + (b == 0 ? 256u * 4u : 0u));
@@ -129,7 +135,6 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
 
         int64_t k = g0 / pt.CG;
         const int64_t kfirst = k;
-        int64_t kend = (k + 1) * pt.CG;
         float sp[W];
         Sum2 acc[W];
 #pragma unroll
@@ -142,11 +147,14 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
             for (int64_t it = 0; it < S && it < items; ++it) issue((int)it, it);
 
         for (int64_t i = 0; i < count; ++i) {
-            const int64_t gi = g0 + i;
-            if (gi == kend) {
-                flush_chunk<W>(pt, q, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
-                ++k;
-                kend += pt.CG;
+            const int64_t gi = g0 + wib + i * wpb;
+            const int64_t kg = gi / pt.CG;
+            if (kg != k) {
+                // this warp's part of chunks k .. kg-1 is done (possibly empty)
+                while (k < kg) {
+                    flush_chunk<W>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+                    ++k;
+                }
 #pragma unroll
                 for (int w = 0; w < W; ++w) sp[w] = __ldg(a.s_prev + (int64_t)w * pt.nchunks + k);
             }
@@ -199,13 +207,17 @@ __global__ void __launch_bounds__(kBlock, 1) k_worker(WorkerArgs a)
                 if (lane == 0 && it + S < items) issue(s, it + S);
             }
         }
-        flush_chunk<W>(pt, q, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+        for (;;) {
+            flush_chunk<W>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+            if (k == klast) break;
+            ++k;
+        }
     }
 }
 
 // Launch shape for (W, gradient type): warps per block and stages per warp chosen so that
 // the stages fill the shared memory of one block (one block per SM): at least two stages
-// per warp, up to eight warps, and as many stages as then fit (at most eight).
+// per warp, up to sixteen warps, and as many stages as then fit (at most eight).
 template <int W, typename G>
 static WorkerConfig config_w(int smem_budget)
 {
@@ -213,9 +225,9 @@ static WorkerConfig config_w(int smem_budget)
     WorkerConfig c{};
     const int usable = smem_budget - (int)kBarBytes;
     int warps = usable / (2 * (int)St::kBytes);
-    warps = warps > 8 ? 8 : (warps < 1 ? 1 : warps);
+    warps = warps > kMaxWarps ? kMaxWarps : (warps < 1 ? 1 : warps);
     int stages = usable / (warps * (int)St::kBytes);
-    stages = stages > 8 ? 8 : (stages < 2 ? 2 : stages);
+    stages = stages > kMaxStages ? kMaxStages : (stages < 2 ? 2 : stages);
     c.warps_per_block = warps;
     c.stages = stages;
     c.smem_bytes = kBarBytes + (size_t)warps * stages * St::kBytes;
