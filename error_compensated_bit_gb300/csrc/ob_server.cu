@@ -56,6 +56,7 @@ template <int W>
 __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 {
     constexpr int T = W < 8 ? W : 8;     // workers covered by the table
+    constexpr int U = W > 8 ? 2 : 1;     // groups per iteration
     __shared__ float s_tab[(kBlock / 32) << T];
     float* tab = s_tab + ((threadIdx.x >> 5) << T);
     const int lane = threadIdx.x & 31;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
         build_average_table<W>(tab, sw, lane);
         Sum2 acc[1] = {{0.0f, 0.0f}};
 
-        for (int64_t gi = g0; gi < g1; ++gi) {
+        for (int64_t gi = g0; gi < g1;) {
             if (gi == kend) {
                 flush_chunk<1>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
                 ++k;
@@ -88,40 +89,53 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
                 tp = __ldg(a.t_prev + k);
                 build_average_table<W>(tab, sw, lane);
             }
-            uint32_t bytes[W];
+            // with W > 8 two groups of a chunk are in flight per iteration
+            const int nu = (U == 2 && gi + 1 < g1 && gi + 1 != kend) ? 2 : 1;
+            uint32_t bytes[U][W];
+            float yv[U][8];
 #pragma unroll
-            for (int w = 0; w < W; ++w) bytes[w] = lane_byte(a.wbits + (int64_t)w * words_per_row, gi, lane);
-            uint64_t lo = 0, hi = 0;
+            for (int u = 0; u < U; ++u) {
+                if (u < nu) {
 #pragma unroll
-            for (int w = 0; w < T; ++w) lo |= (uint64_t)bytes[w] << (8 * w);
-            lo = transpose8x8(lo);
-            if (W > 8) {
-#pragma unroll
-                for (int w = 8; w < W; ++w) hi |= (uint64_t)bytes[w] << (8 * (w - 8));
-                hi = transpose8x8(hi);
-            }
-            const int64_t e0 = gi * 256 + lane * 8;
-            float yv[8];
-            ld8_stream(a.ybuf + e0, yv);
-            uint32_t byte = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float avg = tab[(uint32_t)(lo >> (8 * j)) & 0xffu];
-                if (W > 8) {
-                    const uint32_t pat = (uint32_t)(hi >> (8 * j)) & 0xffu;
-#pragma unroll
-                    for (int w = 8; w < W; ++w) avg = __fadd_rn(avg, signed_scale(sw[w], (pat >> (w - 8)) & 1u));
-                    avg = (W & (W - 1)) == 0 ? __fmul_rn(avg, 1.0f / (float)W) : __fdiv_rn(avg, (float)W);
+                    for (int w = 0; w < W; ++w) bytes[u][w] = lane_byte(a.wbits + (int64_t)w * words_per_row, gi + u, lane);
+                    ld8_stream(a.ybuf + (gi + u) * 256 + lane * 8, yv[u]);
                 }
-                const float es = __fsub_rn(yv[j], signed_scale(tp, yv[j] >= 0.0f));
-                const float y = __fadd_rn(avg, es);
-                yv[j] = y;
-                byte |= (y >= 0.0f ? 1u : 0u) << j;
-                sum2_add_sq(acc[0], y);
             }
-            st8_stream(a.ybuf + e0, yv);
-            const uint32_t word = quad_word(byte, lane);
-            if ((lane & 3) == 0) __stcs(a.sbits + gi * 8 + (lane >> 2), word);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (u < nu) {
+                    const int64_t gu = gi + u;
+                    uint64_t lo = 0, hi = 0;
+#pragma unroll
+                    for (int w = 0; w < T; ++w) lo |= (uint64_t)bytes[u][w] << (8 * w);
+                    lo = transpose8x8(lo);
+                    if (W > 8) {
+#pragma unroll
+                        for (int w = 8; w < W; ++w) hi |= (uint64_t)bytes[u][w] << (8 * (w - 8));
+                        hi = transpose8x8(hi);
+                    }
+                    uint32_t byte = 0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float avg = tab[(uint32_t)(lo >> (8 * j)) & 0xffu];
+                        if (W > 8) {
+                            const uint32_t pat = (uint32_t)(hi >> (8 * j)) & 0xffu;
+#pragma unroll
+                            for (int w = 8; w < W; ++w) avg = __fadd_rn(avg, signed_scale(sw[w], (pat >> (w - 8)) & 1u));
+                            avg = (W & (W - 1)) == 0 ? __fmul_rn(avg, 1.0f / (float)W) : __fdiv_rn(avg, (float)W);
+                        }
+                        const float es = __fsub_rn(yv[u][j], signed_scale(tp, yv[u][j] >= 0.0f));
+                        const float y = __fadd_rn(avg, es);
+                        yv[u][j] = y;
+                        byte |= (y >= 0.0f ? 1u : 0u) << j;
+                        sum2_add_sq(acc[0], y);
+                    }
+                    st8_stream(a.ybuf + gu * 256 + lane * 8, yv[u]);
+                    const uint32_t word = quad_word(byte, lane);
+                    if ((lane & 3) == 0) __stcs(a.sbits + gu * 8 + (lane >> 2), word);
+                }
+            }
+            gi += nu;
         }
         flush_chunk<1>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
@@ -131,13 +145,16 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 // Memory per element: 1/8 (server bits) [+ 1/8 mask bits] + 4 (v) + 8 (x) + 4 (m).
 // Block 0 also moves this step's scales into the "previous" slots for the next step:
 // every kernel that reads the previous slots (worker, server) has finished by now.
+// Groups per warp iteration (all their loads in flight together): four without a mask,
+// two with one (measured faster there: the mask words add loads per group).
+template <bool MASKED>
 __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
 {
-    constexpr int U = 4;   // groups per warp iteration: all their loads are in flight together
+    constexpr int U = MASKED ? 2 : 4;
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const bool masked = a.maskbits != nullptr;
+    constexpr bool masked = MASKED;
     // one contiguous, balanced range of groups per warp (the grid is one resident wave)
     const int64_t g_end = (warp + 1) * a.NG / nwarps;
 
@@ -258,14 +275,17 @@ int occupancy_server(int W)
 
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s)
 {
-    k_update<<<grid, kBlock, 0, s>>>(a);
+    if (a.maskbits) k_update<true><<<grid, kBlock, 0, s>>>(a);
+    else k_update<false><<<grid, kBlock, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 int occupancy_update()
 {
-    int blocks = 0;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_update, kBlock, 0) == cudaSuccess ? blocks : 0;
+    int b0 = 0, b1 = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_update<false>, kBlock, 0) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_update<true>, kBlock, 0) != cudaSuccess) return 0;
+    return b0 < b1 ? b0 : b1;
 }
 
 cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s)
