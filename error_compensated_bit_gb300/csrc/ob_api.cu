@@ -198,6 +198,7 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
     if (W < 1 || W > 16 || n <= 0 || chunk <= 0) return OB_EINVAL;
     if (n % ((int64_t)W * 256) != 0) return OB_EINVAL;
     if (chunk % 256 != 0 || (n / W) % chunk != 0) return OB_EINVAL;
+    if ((int64_t)W * (n / 256) >= (1ll << 32)) return OB_EINVAL;   // group indices fit 32 bits
     if (!finite(b1) || !finite(b2) || !finite(eps) || !finite(lr)) return OB_EINVAL;
     if (b1 < 0.0f || b1 >= 1.0f || b2 < 0.0f || b2 >= 1.0f || eps < 0.0f) return OB_EINVAL;
 
@@ -389,6 +390,7 @@ static int compressed_step_impl(ob_ctx* c, const void* grads, int dtype, float* 
     wa.cnt = at<unsigned>(ws, L.wcnt);
     wa.status = at<unsigned>(ws, L.status);
     wa.pt = c->ptw[dtype];
+    wa.cg_div = make_fastdiv((uint32_t)(c->C / 256));
     wa.n = c->n;
     wa.C = c->C;
     wa.b1 = c->b1;
@@ -431,6 +433,7 @@ static int compressed_step_impl(ob_ctx* c, const void* grads, int dtype, float* 
     ua.CG = c->pts.CG;
     ua.nscales_w = (int64_t)c->W * c->nchunks;
     ua.nchunks = c->nchunks;
+    ua.cg_div = make_fastdiv((uint32_t)(c->C / 256));
     ua.lr = c->lr;
     ua.eps = c->eps;
     ua.wd = c->wd;
@@ -524,6 +527,8 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     a.C = c->C;
     a.nchunks = c->nchunks;
     a.NG = c->n / 256;
+    a.ng_div = make_fastdiv((uint32_t)a.NG);
+    a.cg_div = make_fastdiv((uint32_t)(c->C / 256));
     a.W = c->W;
     a.bits = bits;
     a.beta = beta;
@@ -740,6 +745,7 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
     wa.cnt = cnt;
     wa.status = at<unsigned>(scratch, part_bytes + cnt_bytes);
     wa.pt = pt;
+    wa.cg_div = make_fastdiv((uint32_t)(c->C / 256));
     wa.n = c->n;
     wa.C = c->C;
     wa.b1 = c->b1;

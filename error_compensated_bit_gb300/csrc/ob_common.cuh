@@ -20,6 +20,14 @@ namespace ob {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// n / f.d for 32-bit n (see FastDiv).
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f)
+{
+    if (f.d == 1) return n;
+    const uint32_t t = __umulhi(n, f.m);
+    return (t + ((n - t) >> 1)) >> (f.l - 1);
+}
+
 // ---- range partition ---------------------------------------------------------------------
 
 __device__ __forceinline__ int64_t range_begin(const Part& pt, int64_t q)

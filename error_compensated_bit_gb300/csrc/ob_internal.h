@@ -6,6 +6,25 @@
 
 namespace ob {
 
+// Division by a run-time constant for 32-bit operands, by a precomputed multiplier:
+// n / d == (t + ((n - t) >> 1)) >> (l - 1) with t = high 32 bits of n * m,
+// l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1 (d >= 2; d == 1 is passed through).
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f{d, 0u, 0u};
+    if (d > 1) {
+        uint32_t l = 0;
+        while ((1ull << l) < d) ++l;
+        f.l = l;
+        f.m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+    }
+    return f;
+}
+
 // Partition of the buffer into 256-element groups and P contiguous warp ranges.
 struct Part {
     int64_t NG;       // groups (n / 256)
@@ -25,6 +44,7 @@ struct WorkerArgs {
     double* part;           // [W][P][warps per block][J] partial sums of squares
     unsigned* cnt;          // [nchunks] arrival counters (zero between launches)
     unsigned* status;       // status word (0 = fine; see ob_tma.cuh)
+    FastDiv cg_div;         // division by the groups per chunk
     Part pt;
     int64_t n, C;
     float b1, c1;
@@ -63,6 +83,7 @@ struct UpdateArgs {
     const float* s_next;
     float* t_prev;             // [nchunks] <- t_next
     int64_t NG, CG, nscales_w, nchunks;
+    FastDiv cg_div;            // division by the groups per chunk
     float lr, eps, wd;
 };
 
@@ -104,6 +125,7 @@ struct LocoArgs {
     float* m;
     float* v;
     int64_t n, C, nchunks, NG;
+    FastDiv ng_div, cg_div;    // division by the groups per row / per chunk
     int W, bits;
     float beta, keep, b1, c1, b2, c2, eps, lr, wd;
 };

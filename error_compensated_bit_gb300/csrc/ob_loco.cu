@@ -41,8 +41,8 @@ __global__ void __launch_bounds__(kBlock) k_loco_absmax(LocoArgs a)
     int64_t cur = -1;
     float run = 0.0f;
     for (int64_t t = warp; t < groups; t += nwarps) {
-        const int64_t w = t / a.NG, gi = t % a.NG;
-        const int64_t key = w * a.nchunks + gi / CG;
+        const int64_t w = fast_div((uint32_t)t, a.ng_div), gi = t - w * a.NG;
+        const int64_t key = w * a.nchunks + fast_div((uint32_t)gi, a.cg_div);
         if (key != cur) {
             const float mx = warp_max(run);
             if (cur >= 0 && lane == 0) atomicMax(a.amax_bits + cur, __float_as_uint(mx));
@@ -71,10 +71,10 @@ __global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
     const float L = (float)((1 << (BITS - 1)) - 1);
     const int64_t row_bytes = a.n * BITS / 8;
     for (int64_t t = warp; t < groups; t += nwarps) {
-        const int64_t w = t / a.NG, gi = t % a.NG;
-        const int64_t k = gi / CG;
+        const int64_t w = fast_div((uint32_t)t, a.ng_div), gi = t - w * a.NG;
+        const int64_t k = fast_div((uint32_t)gi, a.cg_div);
         const float s = __fdiv_rn(__uint_as_float(__ldcg(a.amax_bits + w * a.nchunks + k)), L);
-        if (lane == 0 && gi % CG == 0) a.scale[w * a.nchunks + k] = s;
+        if (lane == 0 && gi == k * CG) a.scale[w * a.nchunks + k] = s;
         const int64_t e0 = gi * 256 + lane * 8;
         float gv[8], ev[8];
         Grad<G>::ld8(a.g, w * a.n + e0, gv);
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kBlock) k_loco_server(LocoArgs a)
     for (int64_t i8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i8 < nvec;
          i8 += (int64_t)gridDim.x * blockDim.x) {
         const int64_t e0 = i8 * 8;
-        const int64_t k = e0 / a.C;
+        const int64_t k = fast_div((uint32_t)(i8 >> 5), a.cg_div);   // e0 / C
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;

@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
             const int64_t gi = gb + u;
             if (gi < g_end) {
                 const int64_t e0 = gi * 256 + lane * 8;
-                T[u] = __ldg(a.t_next + gi / a.CG);
+                T[u] = __ldg(a.t_next + fast_div((uint32_t)gi, a.cg_div));
                 sb[u] = lane_byte(a.sbits, gi, lane);
                 mb[u] = masked ? lane_byte(a.maskbits, gi, lane) : 0xffu;
                 ld8_stream(a.v + e0, vv[u]);

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
 
         for (int64_t i = 0; i < count; ++i) {
             const int64_t gi = g0 + wib + i * wpb;
-            const int64_t kg = gi / pt.CG;
+            const int64_t kg = fast_div((uint32_t)gi, a.cg_div);
             if (kg != k) {
                 // this warp's part of chunks k .. kg-1 is done (possibly empty)
                 while (k < kg) {

@@ -24,7 +24,8 @@
  *
  * Conventions shared by every entry point:
  *   - n      elements of the flat parameter buffer; n % (W*256) == 0 (pad the buffer:
- *            pad elements with g = 0, x = 0, m = 0, v = 1 behave like any other).
+ *            pad elements with g = 0, x = 0, m = 0, v = 1 behave like any other), and
+ *            W*n < 2^40 (every 256-element group of every row is numbered in 32 bits).
  *   - W      simulated workers, 1..16.
  *   - chunk  elements per scale; chunk % 256 == 0 and (n/W) % chunk == 0. Chunk k is
  *            elements [k*chunk, (k+1)*chunk), the same chunks for workers and servers.

@@ -57,7 +57,7 @@ def _init(ob, n=1 << 20, W=4, chunk=1 << 18, b1=0.9, b2=0.999, eps=1e-8, lr=1e-4
 @pytest.mark.parametrize("kw", [
     dict(W=0), dict(W=17), dict(n=1000), dict(n=(1 << 20) + 256), dict(chunk=300),
     dict(chunk=3 << 18), dict(n=0), dict(lr=float("nan")), dict(b1=1.0), dict(b2=-0.1),
-    dict(eps=-1.0), dict(chunk=0)])
+    dict(eps=-1.0), dict(chunk=0), dict(n=1 << 36, W=16, chunk=1 << 20)])
 def test_init_rejects(ob, kw):
     rc, h = _init(ob, **kw)
     assert rc == ob.OB_EINVAL and not h.value
