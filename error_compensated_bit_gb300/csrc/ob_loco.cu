@@ -69,11 +69,13 @@ __global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
     const int64_t groups = (int64_t)a.W * a.NG;
     const int64_t CG = a.C / 256;
     const float L = (float)((1 << (BITS - 1)) - 1);
+    constexpr float kTieMargin = (float)(1 << (BITS - 1)) * 0x1p-21f;   // (L + 1) 2^-21
     const int64_t row_bytes = a.n * BITS / 8;
     for (int64_t t = warp; t < groups; t += nwarps) {
         const int64_t w = fast_div((uint32_t)t, a.ng_div), gi = t - w * a.NG;
         const int64_t k = fast_div((uint32_t)gi, a.cg_div);
         const float s = __fdiv_rn(__uint_as_float(__ldcg(a.amax_bits + w * a.nchunks + k)), L);
+        const float inv = __frcp_rn(s);
         if (lane == 0 && gi == k * CG) a.scale[w * a.nchunks + k] = s;
         const int64_t e0 = gi * 256 + lane * 8;
         float gv[8], ev[8];
@@ -85,7 +87,14 @@ __global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
             const float c = __fadd_rn(gv[j], ev[j]);
             int qi = 0;
             if (s > 0.0f) {
-                float r = rintf(__fdiv_rn(c, s));
+                // rint(c/s) with c/s correctly rounded, as defined. |c/s| <= L(1+u), and
+                // c * rn(1/s) lies within 3u|c/s| < (L+1) 2^-22 of rn(c/s); unless it is
+                // that close to a half-integer, both round to the same integer. Near a
+                // half-integer (the test keeps twice that distance) or when 1/s overflows,
+                // the quotient is formed exactly.
+                const float qq = __fmul_rn(c, inv);
+                float r = rintf(qq);
+                if (!(fabsf(__fsub_rn(qq, r)) < 0.5f - kTieMargin)) r = rintf(__fdiv_rn(c, s));
                 r = fminf(fmaxf(r, -L), L);
                 qi = (int)r;
             }
