@@ -19,7 +19,7 @@ a bounded sample of the same workload.
 With --gpus N > 1 (launched by torchrun) every rank runs an independent replica on its
 own GPU (the path does not shard: the W workers already live on one GPU); the value is
 the units of all ranks over the slowest rank's time. --impl reference times the CPU
-oracle (the reference implementation of this build) on the same workload.
+oracle (the reference the kernels are checked against) on the same workload.
 """
 import argparse
 import hashlib

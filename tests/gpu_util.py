@@ -50,7 +50,7 @@ def unpack_bits(words, n):
     return b.reshape(*w.shape[:-1], n).astype(bool)
 
 
-class GpuRun:
+class CudaPath:
     """The CUDA path on one device, holding the state as torch tensors."""
 
     def __init__(self, st, device="cuda", mask=None):

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_util import GpuRun, Tracker, assert_close, exact_fraction, random_state, unpack_bits
+from gpu_util import CudaPath, Tracker, assert_close, exact_fraction, random_state, unpack_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def _grads(rng, W, n, dtype, scale=1e-3):
 
 
 def _free_run(ora, st, grads_fn, steps, mask=None):
-    gpu = GpuRun(st, mask=mask)
+    gpu = CudaPath(st, mask=mask)
     tr = Tracker(st.n, st.W, st.C)
     fracs = []
     for t in range(steps):
@@ -131,7 +131,7 @@ def test_edge_cases(ora, case):
         st.mask = np.zeros(n, np.uint8)
     elif case == "huge_range":
         g = _grads(rng, W, n, "f32") * np.float32(10.0) ** rng.integers(-12, 6, (W, n)).astype(np.float32)
-    gpu = GpuRun(st, mask=mask)
+    gpu = CudaPath(st, mask=mask)
     tr = Tracker(n, W, C)
     for t in range(3):
         out = ora.compressed_step(st, g)
@@ -149,7 +149,7 @@ def test_deterministic(ora):
     g = _grads(rng, W, n, "f16")
     snaps = []
     for rep in range(2):
-        gpu = GpuRun(st.copy())
+        gpu = CudaPath(st.copy())
         for t in range(3):
             gpu.compressed_step(g)
         snaps.append(gpu.snapshot())
@@ -163,7 +163,7 @@ def test_reset_and_export(ora):
     W, n = 4, 4 * 256 * 200
     C = n // W // 2
     st = random_state(rng, n, W, C)
-    gpu = GpuRun(st)
+    gpu = CudaPath(st)
     tr = Tracker(n, W, C)
     for t in range(2):
         g = _grads(rng, W, n, "f32")
@@ -187,7 +187,7 @@ def test_warmup_parity(ora, W, dtype, bc, wd):
     rng = np.random.default_rng(20 + W)
     n = W * 256 * 333
     st = random_state(rng, n, W, n // W, v_dist="lognormal", wd=wd)
-    gpu = GpuRun(st)
+    gpu = CudaPath(st)
     gpu.ctx.set_options(wd, bc)
     for t in range(4):
         g = _grads(rng, W, n, dtype)
@@ -207,7 +207,7 @@ def test_warmup_then_compressed(ora):
     zero = rng.random(n) < 0.02
     mask = (~zero).astype(np.float32)
     st = random_state(rng, n, W, n // W, v_dist="lognormal", mask=mask)
-    gpu = GpuRun(st, mask=mask)
+    gpu = CudaPath(st, mask=mask)
     tr = Tracker(n, W, n // W)
     for t in range(7):
         g = _grads(rng, W, n, "f32")
@@ -229,7 +229,7 @@ def test_loco_parity(ora, W, dtype, bits):
     C = n // W // 2
     st = random_state(rng, n, W, C)
     st.v[:] = 0.0
-    gpu = GpuRun(st)
+    gpu = CudaPath(st)
     err_d = torch.zeros(W, n, dtype=torch.float32, device="cuda")
     lws = torch.zeros(gpu.ctx.loco_workspace_bytes(bits), dtype=torch.uint8, device="cuda")
     err = np.zeros((W, n), np.float32)
@@ -280,7 +280,7 @@ def test_host_buffer_entry_point_matches_device_path():
     W, n = 4, 4 * 256 * 300
     C = n // W
     st = random_state(rng, n, W, C)
-    a, b = GpuRun(st.copy()), GpuRun(st.copy())
+    a, b = CudaPath(st.copy()), CudaPath(st.copy())
     grads = [torch.from_numpy(_grads(rng, W, n, "f16")) for _ in range(3)]
     hosts = [g.pin_memory() for g in grads]
     dev_bufs = [torch.empty(W, n, dtype=torch.float16, device="cuda") for _ in range(2)]
