@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--graph", action="store_true",
+                   help="time replays of one step captured in a CUDA graph (small, launch-bound buffers)")
     return p.parse_args()
 
 
@@ -301,6 +303,21 @@ def gpu_arm(args, wl):
     for _ in range(max(3, args.warmup)):
         one_step()
     torch.cuda.synchronize(dev)
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            cap = torch.cuda.current_stream(dev)
+            if args.phase == "compressed":
+                ctx.compressed_step(g, x, m, v, ew, es, ws, cap)
+            elif args.phase == "warmup":
+                ctx.warmup_step(g, x, m, v, ws, cap)
+            else:
+                ctx.loco_step(g, x, m, v, ew, lws, 0.9, 4, cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
 
     # timed region
     clocks = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else
@@ -315,13 +332,18 @@ def gpu_arm(args, wl):
     time.sleep(0.3)
     ev0.record(stream)
     for _ in range(args.steps):
-        one_step()
+        if graph is not None:
+            graph.replay()
+        else:
+            one_step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier(dist)
     ms_total = ev0.elapsed_time(ev1)
     launches = ctx.launch_count() - launches0
+    if graph is not None:     # replays launch the captured kernels without the library's counter
+        launches = args.steps * {"compressed": 3, "warmup": 1, "loco": 3}[args.phase]
     kid = {"compressed": ob.OB_K_WORKER, "warmup": ob.OB_K_WARMUP, "loco": ob.OB_K_LOCO_QUANT}[args.phase]
     k_ms, k_n = ctx.profile_read(kid)
     per_kernel = {}
@@ -347,8 +369,9 @@ def gpu_arm(args, wl):
     else:
         k_bytes = n * W * (s_g + 8.5)
         khash = kernel_source_hash(["ob_loco.cu", "ob_common.cuh"])
-    k_avg_s = (k_ms / k_n) / 1e3 if k_n else float("nan")
-    achieved = k_bytes / k_avg_s / 1e9
+    # per-kernel events exist only for direct launches (not for graph replays)
+    k_avg_s = (k_ms / k_n) / 1e3 if k_n else None
+    achieved = k_bytes / k_avg_s / 1e9 if k_avg_s else None
     traffic = load_traffic(wl.name, W, khash) if args.phase == "compressed" else None
 
     # end to end through the host-buffer entry point (compressed phase only)
@@ -387,14 +410,15 @@ def gpu_arm(args, wl):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(wl, args.phase), "n": n, "W": W, "chunk": C,
                    "grad_dtype": str(wl.grad_dtype).split(".")[-1], "masked": masked,
+                   "cuda_graph": graph is not None,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "no flush: each step streams %.1f GB, far more than the 129 MB L2" % (b_step / 1e9)},
         "hbm_gbs_step": b_step / (ms_step / 1e3) / 1e9,
         "hbm_frac_step": b_step / (ms_step / 1e3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak if achieved else None, "traffic": traffic,
                      "kernel": {"compressed": "worker", "warmup": "warmup", "loco": "loco_quant"}[args.phase],
-                     "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_avg_s * 1e6,
+                     "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_avg_s * 1e6 if k_avg_s else None,
                      "peak_kind": "%s hbm_gbs (STREAM-style copy)" % peak_kind},
         "kernels": per_kernel,
         "clocks": clk, "gpu_launches": launches, "e2e": e2e,

@@ -190,9 +190,75 @@ static __device__ __noinline__ double chunk_sumsq_exact(const float* row, int64_
 // counter is reset for the next launch. A range q is worked by `wpr` warps (warp `wir`
 // of them here), each of which flushes one partial -- possibly zero -- for every chunk
 // the range touches, so chunk k has (ranges touching it) * wpr contributors, combined
-// range by range, warp by warp. `rows` is the buffer the squares came from (row r at
+// range by range, warp by warp (at most 16 warps per range). `rows` is the buffer the squares came from (row r at
 // rows + r*row_stride), read only on the degenerate slow path.
+// The last contributor of chunk k combines the chunk's partials and writes its scales.
 template <int R>
+__device__ __forceinline__ void finalize_chunk_body(const Part& pt, int wpr, int64_t k, const double* part,
+                                            unsigned* cnt, float* scale_out, int64_t C,
+                                            const float* rows, int64_t row_stride, int lane)
+{
+    __threadfence();
+    int64_t lo, hi;
+    chunk_contributors(pt, k, lo, hi);
+    if (wpr == 1) {
+        // one warp per range: lanes take the ranges in turn
+        for (int r = 0; r < R; ++r) {
+            double sum = 0.0;
+            for (int64_t qq = lo + lane; qq <= hi; qq += 32) {
+                const int64_t jj = k - range_begin(pt, qq) / pt.CG;
+                sum += __ldcg(part + ((int64_t)r * pt.P + qq) * pt.J + jj);
+            }
+            sum = warp_sum(sum);
+            if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
+            if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(sum / (double)C);
+        }
+    } else {
+        // several warps per range: walk the ranges in order (the chunk's slot in a range is
+        // computed once per range); lane l owns the (row, warp) pairs l, l+32, ... and keeps
+        // one running sum per pair; per-row totals are then formed in a fixed order.
+        constexpr int kSlots = (R * 16 + 31) / 32;   // pairs per lane (wpr <= 16)
+        const int pairs = R * wpr;
+        double acc_p[kSlots];
+        int row_of[kSlots];
+        int64_t off_of[kSlots];
+#pragma unroll
+        for (int i = 0; i < kSlots; ++i) {
+            const int pi = lane + 32 * i;
+            acc_p[i] = 0.0;
+            row_of[i] = pi < pairs ? pi / wpr : -1;
+            off_of[i] = pi < pairs ? ((int64_t)(pi / wpr) * pt.P * wpr + pi % wpr) * pt.J : 0;
+        }
+        for (int64_t qq = lo; qq <= hi; ++qq) {
+            const int64_t base = qq * wpr * pt.J + (k - range_begin(pt, qq) / pt.CG);
+#pragma unroll
+            for (int i = 0; i < kSlots; ++i)
+                if (row_of[i] >= 0) acc_p[i] += __ldcg(part + off_of[i] + base);
+        }
+        for (int r = 0; r < R; ++r) {
+            double v = 0.0;
+#pragma unroll
+            for (int i = 0; i < kSlots; ++i)
+                if (row_of[i] == r) v += acc_p[i];
+            double sum = warp_sum(v);
+            if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
+            if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(sum / (double)C);
+        }
+    }
+    if (lane == 0) cnt[k] = 0u;
+}
+
+// Out of line, so that a register-hungry kernel does not carry the combination's
+// registers through its streaming loop (it runs once per chunk); inline for the rest.
+template <int R>
+__device__ __noinline__ void finalize_chunk_outlined(const Part& pt, int wpr, int64_t k, const double* part,
+                                                     unsigned* cnt, float* scale_out, int64_t C,
+                                                     const float* rows, int64_t row_stride, int lane)
+{
+    finalize_chunk_body<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
+}
+
+template <int R, bool OUTLINE>
 __device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, int wir, int64_t k,
                                             int64_t kfirst, Sum2 (&acc)[R], double* part,
                                             unsigned* cnt, float* scale_out, int64_t C,
@@ -215,23 +281,10 @@ __device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, 
         last = (prev == (unsigned)((hi - lo + 1) * wpr - 1)) ? 1u : 0u;
     }
     last = __shfl_sync(kFull, last, 0);
-    if (!last) return;
-    __threadfence();
-    int64_t lo, hi;
-    chunk_contributors(pt, k, lo, hi);
-    const int64_t total = (hi - lo + 1) * wpr;
-    for (int r = 0; r < R; ++r) {
-        double sum = 0.0;
-        for (int64_t t = lane; t < total; t += 32) {
-            const int64_t qq = lo + t / wpr;
-            const int64_t jj = k - range_begin(pt, qq) / pt.CG;
-            sum += __ldcg(part + (((int64_t)r * pt.P + qq) * wpr + t % wpr) * pt.J + jj);
-        }
-        sum = warp_sum(sum);
-        if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
-        if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(sum / (double)C);
+    if (last) {
+        if (OUTLINE) finalize_chunk_outlined<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
+        else finalize_chunk_body<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
     }
-    if (lane == 0) cnt[k] = 0u;
 }
 
 }  // namespace ob

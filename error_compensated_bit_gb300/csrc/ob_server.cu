@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 
         for (int64_t gi = g0; gi < g1;) {
             if (gi == kend) {
-                flush_chunk<1>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+                flush_chunk<1, (W > 8)>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
                 ++k;
                 kend += pt.CG;
 #pragma unroll
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
             }
             gi += nu;
         }
-        flush_chunk<1>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+        flush_chunk<1, (W > 8)>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
 }
 

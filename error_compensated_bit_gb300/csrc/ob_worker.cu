@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
             if (kg != k) {
                 // this warp's part of chunks k .. kg-1 is done (possibly empty)
                 while (k < kg) {
-                    flush_chunk<W>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+                    flush_chunk<W, true>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
                     ++k;
                 }
 #pragma unroll
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
             }
         }
         for (;;) {
-            flush_chunk<W>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+            flush_chunk<W, true>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
             if (k == klast) break;
             ++k;
         }

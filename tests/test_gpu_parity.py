@@ -297,3 +297,27 @@ def test_host_buffer_entry_point_matches_device_path():
         assert np.array_equal(sb_host.numpy().view(np.uint32), sb_["sbits"])
         assert np.array_equal(ss_host.numpy(), sb_["sscale"])
     assert b.ctx.read_status(b.ws) == 0
+
+
+def test_compressed_step_replays_from_a_cuda_graph(ora):
+    """One compressed step captured into a CUDA graph and replayed gives, step for step,
+    exactly what eager calls give (launch-bound small buffers can be run this way)."""
+    rng = np.random.default_rng(80)
+    W, n = 4, 4 * 256 * 128
+    st = random_state(rng, n, W, n // W)
+    g = torch.from_numpy(_grads(rng, W, n, "f16")).cuda()
+    eager, graphed = CudaPath(st.copy()), CudaPath(st.copy())
+    graphed.compressed_step(g)                    # first call outside the capture
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        graphed.ctx.compressed_step(g, graphed.x, graphed.m, graphed.v, graphed.ew, graphed.es, graphed.ws)
+    eager.compressed_step(g)
+    for t in range(3):
+        graph.replay()
+        eager.compressed_step(g)
+        torch.cuda.synchronize()
+        a, b = eager.snapshot(), graphed.snapshot()
+        for k in ("wbits", "wscale", "sbits", "sscale", "x", "m", "z", "y"):
+            assert np.array_equal(np.asarray(a[k]).view(np.uint8), np.asarray(b[k]).view(np.uint8)), (t, k)
