@@ -308,6 +308,7 @@ def gpu_arm(args, wl):
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
+        cap0 = ctx.launch_count()
         with torch.cuda.graph(graph, stream=side):
             cap = torch.cuda.current_stream(dev)
             if args.phase == "compressed":
@@ -316,6 +317,7 @@ def gpu_arm(args, wl):
                 ctx.warmup_step(g, x, m, v, ws, cap)
             else:
                 ctx.loco_step(g, x, m, v, ew, lws, 0.9, 4, cap)
+        graph_launches = ctx.launch_count() - cap0     # kernels captured per step
         graph.replay()
         torch.cuda.synchronize(dev)
 
@@ -343,7 +345,7 @@ def gpu_arm(args, wl):
     ms_total = ev0.elapsed_time(ev1)
     launches = ctx.launch_count() - launches0
     if graph is not None:     # replays launch the captured kernels without the library's counter
-        launches = args.steps * {"compressed": 3, "warmup": 1, "loco": 3}[args.phase]
+        launches = args.steps * graph_launches
     kid = {"compressed": ob.OB_K_WORKER, "warmup": ob.OB_K_WARMUP, "loco": ob.OB_K_LOCO_QUANT}[args.phase]
     k_ms, k_n = ctx.profile_read(kid)
     per_kernel = {}

@@ -41,7 +41,8 @@ struct ob_ctx {
     int device = -1;
     int sms = 152;
     int smem_budget = 232448;   // opt-in shared memory per block
-    Part ptw[3]{};              // worker partition per gradient type (one warp per range)
+    Part ptw[3]{};              // worker partition per gradient type
+    int wpr[3]{};               // worker warps per range (warps per block, or 1)
     Part pts{};                 // server partition
     int grid_s = 0;
     int grid_u = 0;             // update kernel: one resident wave
@@ -232,8 +233,17 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
     int64_t wpart = 0;
     for (int dt = 0; dt < 3; ++dt) {
         const WorkerConfig wc = worker_config(W, dt, c->smem_budget);
-        c->ptw[dt] = make_part(n, chunk, (int64_t)c->sms);      // one range per block
-        const int64_t need = (int64_t)W * c->ptw[dt].P * wc.warps_per_block * c->ptw[dt].J;
+        // one range per block with interleaved warps while a block range spans at most a
+        // couple of chunks; one range per warp for short chunks
+        Part blocks = make_part(n, chunk, (int64_t)c->sms);
+        if (blocks.J <= 2) {
+            c->ptw[dt] = blocks;
+            c->wpr[dt] = wc.warps_per_block;
+        } else {
+            c->ptw[dt] = make_part(n, chunk, (int64_t)c->sms * wc.warps_per_block);
+            c->wpr[dt] = 1;
+        }
+        const int64_t need = (int64_t)W * c->ptw[dt].P * c->wpr[dt] * c->ptw[dt].J;
         if (need > wpart) wpart = need;
     }
     // server: all resident blocks, a power of two per SM
@@ -390,6 +400,7 @@ static int compressed_step_impl(ob_ctx* c, const void* grads, int dtype, float* 
     wa.cnt = at<unsigned>(ws, L.wcnt);
     wa.status = at<unsigned>(ws, L.status);
     wa.pt = c->ptw[dtype];
+    wa.interleave = c->wpr[dtype] > 1 ? 1 : 0;
     wa.cg_div = make_fastdiv((uint32_t)(c->C / 256));
     wa.n = c->n;
     wa.C = c->C;
@@ -437,7 +448,13 @@ static int compressed_step_impl(ob_ctx* c, const void* grads, int dtype, float* 
     ua.lr = c->lr;
     ua.eps = c->eps;
     ua.wd = c->wd;
+    // the update's first block moves a few scales itself; many get a kernel of their own
+    const UpdateArgs moves = ua;
+    const bool many = ua.nscales_w + ua.nchunks > 16 * kBlock;
+    if (many) ua.nscales_w = ua.nchunks = 0;
     if (int r = launch(c, OB_K_UPDATE, s, [&] { return launch_update(ua, c->grid_u, s); })) return r;
+    if (many)
+        if (int r = launch(c, OB_K_SCALES, s, [&] { return launch_scales(moves, stream_grid(c), s); })) return r;
     c->step += 1;
     return OB_OK;
 }
@@ -718,10 +735,9 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
                           (const void*)wbits, (const void*)scale_out})
         if (int r = check_ptr(p, 16)) return r;
     if (scale_prev == scale_out) return OB_EINVAL;
-    // scratch: partial sums [W][P][J] doubles, then one counter per chunk
+    // scratch: partial sums [W][P][warps per range][J] doubles, then one counter per chunk
     const Part& pt = c->ptw[dtype];
-    const int wpb = worker_config(c->W, dtype, c->smem_budget).warps_per_block;
-    const size_t part_bytes = up((size_t)c->W * pt.P * wpb * pt.J * 8, kAlignWs);
+    const size_t part_bytes = up((size_t)c->W * pt.P * c->wpr[dtype] * pt.J * 8, kAlignWs);
     const size_t cnt_bytes = up((size_t)c->nchunks * 4, 16);
     if (part_bytes + cnt_bytes + 16 > (size_t)OB_NOALLOC_SCRATCH_BYTES) return OB_ESCRATCH;
     if (int r = check_device(c)) return r;
@@ -745,6 +761,7 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
     wa.cnt = cnt;
     wa.status = at<unsigned>(scratch, part_bytes + cnt_bytes);
     wa.pt = pt;
+    wa.interleave = c->wpr[dtype] > 1 ? 1 : 0;
     wa.cg_div = make_fastdiv((uint32_t)(c->C / 256));
     wa.n = c->n;
     wa.C = c->C;

@@ -184,57 +184,90 @@ static __device__ __noinline__ double chunk_sumsq_exact(const float* row, int64_
     return warp_sum(acc);
 }
 
-// Flush this warp's sums of squares for chunk k (rows 0..R-1), and, if this warp is
-// the last contributor of chunk k, combine all contributors' partials in a fixed order
-// and write the chunk's RMS scales. No waiting: the last arrival does the work; the
-// counter is reset for the next launch. A range q is worked by `wpr` warps (warp `wir`
-// of them here), each of which flushes one partial -- possibly zero -- for every chunk
-// the range touches, so chunk k has (ranges touching it) * wpr contributors, combined
-// range by range, warp by warp (at most 16 warps per range). `rows` is the buffer the squares came from (row r at
-// rows + r*row_stride), read only on the degenerate slow path.
-// The last contributor of chunk k combines the chunk's partials and writes its scales.
+// ---- per-chunk scales from partial sums ------------------------------------------------------
+//
+// A range q is worked by `wpr` warps (warp `wir` of them here); each flushes one double
+// partial per row -- possibly zero -- for every chunk the range touches, into slot
+//   part[((r * P + q) * wpr + wir) * J + j],   j = k - (first chunk of range q).
+// Chunk k is touched by ranges lo..hi: range lo holds the chunk's first group (its slot is
+// j = k - first chunk of lo), and every later one starts inside chunk k (slot j = 0). No
+// warp waits on another: the last arrival combines, writes the chunk's RMS scales and
+// resets the chunk's counter for the next launch. `rows` is the buffer the squares came
+// from (row r at rows + r*row_stride), read only on the degenerate slow path.
+
+// The last contributor's combination: every row's partials added range by range, warp by
+// warp (a lane's running sums add their terms in ascending range order; the 32 lanes' sums
+// are then combined by a fixed butterfly), then scale = sqrt(sum / C). Loads of several
+// ranges are issued before they are added; a missing term adds +0.0, which leaves a sum of
+// squares unchanged, so the unrolling does not change the result.
 template <int R>
-__device__ __forceinline__ void finalize_chunk_body(const Part& pt, int wpr, int64_t k, const double* part,
-                                            unsigned* cnt, float* scale_out, int64_t C,
-                                            const float* rows, int64_t row_stride, int lane)
+__device__ __forceinline__ void combine_chunk(const Part& pt, int wpr, int64_t k, const double* part,
+                                              unsigned* cnt, float* scale_out, int64_t C,
+                                              const float* rows, int64_t row_stride, int lane)
 {
-    __threadfence();
     int64_t lo, hi;
     chunk_contributors(pt, k, lo, hi);
+    const int64_t jlo = k - range_begin(pt, lo) / pt.CG;
     if (wpr == 1) {
-        // one warp per range: lanes take the ranges in turn
-        for (int r = 0; r < R; ++r) {
-            double sum = 0.0;
-            for (int64_t qq = lo + lane; qq <= hi; qq += 32) {
-                const int64_t jj = k - range_begin(pt, qq) / pt.CG;
-                sum += __ldcg(part + ((int64_t)r * pt.P + qq) * pt.J + jj);
+        // lanes take the ranges in turn, all rows at once
+        constexpr int U = R == 1 ? 4 : (R <= 4 ? 2 : 1);
+        double acc_r[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc_r[r] = 0.0;
+        for (int64_t q0 = lo + lane; q0 <= hi; q0 += 32 * U) {
+            double v[U][R];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t qq = q0 + 32 * u;
+                const int64_t off = qq * pt.J + (qq == lo ? jlo : 0);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    v[u][r] = qq <= hi ? __ldcg(part + (int64_t)r * pt.P * pt.J + off) : 0.0;
             }
-            sum = warp_sum(sum);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < R; ++r) acc_r[r] += v[u][r];
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            double sum = warp_sum(acc_r[r]);
             if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
             if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(sum / (double)C);
         }
     } else {
-        // several warps per range: walk the ranges in order (the chunk's slot in a range is
-        // computed once per range); lane l owns the (row, warp) pairs l, l+32, ... and keeps
-        // one running sum per pair; per-row totals are then formed in a fixed order.
+        // several warps per range: lane l owns the (row, warp) pairs l, l+32, ... and adds
+        // that pair's partials range by range; per-row totals are then formed in a fixed order
         constexpr int kSlots = (R * 16 + 31) / 32;   // pairs per lane (wpr <= 16)
+        constexpr int U = kSlots <= 2 ? 4 : 2;
         const int pairs = R * wpr;
+        const int64_t range_stride = (int64_t)wpr * pt.J;
         double acc_p[kSlots];
         int row_of[kSlots];
-        int64_t off_of[kSlots];
+        int64_t base_of[kSlots];
 #pragma unroll
         for (int i = 0; i < kSlots; ++i) {
             const int pi = lane + 32 * i;
             acc_p[i] = 0.0;
             row_of[i] = pi < pairs ? pi / wpr : -1;
-            off_of[i] = pi < pairs ? ((int64_t)(pi / wpr) * pt.P * wpr + pi % wpr) * pt.J : 0;
+            base_of[i] = pi < pairs ? ((int64_t)(pi / wpr) * pt.P * wpr + pi % wpr) * pt.J : 0;
         }
-        for (int64_t qq = lo; qq <= hi; ++qq) {
-            const int64_t base = qq * wpr * pt.J + (k - range_begin(pt, qq) / pt.CG);
+        for (int64_t q0 = lo; q0 <= hi; q0 += U) {
+            double v[U][kSlots];
 #pragma unroll
-            for (int i = 0; i < kSlots; ++i)
-                if (row_of[i] >= 0) acc_p[i] += __ldcg(part + off_of[i] + base);
+            for (int u = 0; u < U; ++u) {
+                const int64_t qq = q0 + u;
+                const int64_t off = qq * range_stride + (qq == lo ? jlo : 0);
+#pragma unroll
+                for (int i = 0; i < kSlots; ++i)
+                    v[u][i] = (qq <= hi && row_of[i] >= 0) ? __ldcg(part + base_of[i] + off) : 0.0;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int i = 0; i < kSlots; ++i) acc_p[i] += v[u][i];
         }
+#pragma unroll
         for (int r = 0; r < R; ++r) {
             double v = 0.0;
 #pragma unroll
@@ -248,29 +281,39 @@ __device__ __forceinline__ void finalize_chunk_body(const Part& pt, int wpr, int
     if (lane == 0) cnt[k] = 0u;
 }
 
-// Out of line, so that a register-hungry kernel does not carry the combination's
-// registers through its streaming loop (it runs once per chunk); inline for the rest.
+// Scales of a chunk whose only contributor is this warp (a chunk that lies wholly inside
+// the range of a warp working alone): its partial is the chunk's total -- the combination
+// would only add zeros to it -- so the scales are written at once, with no fence and no
+// counter. Lane 0 has stored the partials (row r's at idx0 + r*P*J); lane r reads row r's
+// back and forms its scale, all rows at once.
 template <int R>
-__device__ __noinline__ void finalize_chunk_outlined(const Part& pt, int wpr, int64_t k, const double* part,
-                                                     unsigned* cnt, float* scale_out, int64_t C,
-                                                     const float* rows, int64_t row_stride, int lane)
+__device__ __forceinline__ void sole_chunk(const Part& pt, int64_t k, const double* part, int64_t idx0,
+                                           float* scale_out, int64_t C, const float* rows,
+                                           int64_t row_stride, int lane)
 {
-    finalize_chunk_body<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
+    __syncwarp();                   // orders lane 0's stores before the other lanes' loads
+    double mine = lane < R ? __ldcg(part + idx0 + (int64_t)lane * pt.P * pt.J) : 0.0;
+    unsigned bad = __ballot_sync(kFull, lane < R && !sumsq_trusted(mine, C));
+    if (bad) __threadfence();       // the chunk's rows were just stored by this warp's lanes
+    while (bad) {
+        const int r = __ffs(bad) - 1;
+        bad &= bad - 1;
+        const double ex = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
+        if (lane == r) mine = ex;
+    }
+    if (lane < R) scale_out[(int64_t)lane * pt.nchunks + k] = (float)sqrt(mine / (double)C);
 }
 
-template <int R, bool OUTLINE>
-__device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, int wir, int64_t k,
-                                            int64_t kfirst, Sum2 (&acc)[R], double* part,
-                                            unsigned* cnt, float* scale_out, int64_t C,
-                                            const float* rows, int64_t row_stride, int lane)
+// After the partials are stored: the only contributor writes the scales; any other counts
+// itself in, and the last one combines.
+template <int R>
+__device__ __forceinline__ void flush_rest(const Part& pt, int wpr, int64_t k, bool sole, int64_t idx0,
+                                           double* part, unsigned* cnt, float* scale_out, int64_t C,
+                                           const float* rows, int64_t row_stride, int lane)
 {
-    const int64_t j = k - kfirst;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
-        if (lane == 0) part[(((int64_t)r * pt.P + q) * wpr + wir) * pt.J + j] = d;
-        acc[r].s = 0.0f;
-        acc[r].e = 0.0f;
+    if (sole) {
+        sole_chunk<R>(pt, k, part, idx0, scale_out, C, rows, row_stride, lane);
+        return;
     }
     __threadfence();
     unsigned last = 0;
@@ -281,9 +324,69 @@ __device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, 
         last = (prev == (unsigned)((hi - lo + 1) * wpr - 1)) ? 1u : 0u;
     }
     last = __shfl_sync(kFull, last, 0);
-    if (last) {
-        if (OUTLINE) finalize_chunk_outlined<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
-        else finalize_chunk_body<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
+    if (last) combine_chunk<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
+}
+
+// Out-of-line forms, so that a register-hungry kernel does not carry this code's
+// registers through its streaming loop (it runs once per chunk and range).
+template <int R>
+__device__ __noinline__ void flush_rest_outlined(const Part& pt, int wpr, int64_t k, bool sole, int64_t idx0,
+                                                 double* part, unsigned* cnt, float* scale_out, int64_t C,
+                                                 const float* rows, int64_t row_stride, int lane)
+{
+    flush_rest<R>(pt, wpr, k, sole, idx0, part, cnt, scale_out, C, rows, row_stride, lane);
+}
+
+template <int R>
+__device__ __noinline__ void combine_chunk_outlined(const Part& pt, int wpr, int64_t k, const double* part,
+                                                    unsigned* cnt, float* scale_out, int64_t C,
+                                                    const float* rows, int64_t row_stride, int lane)
+{
+    combine_chunk<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
+}
+
+// How flush_chunk's rarely run part is laid out; the best choice depends on the calling
+// kernel's register pressure (measured per kernel).
+enum FlushCode {
+    kFlushInline,       // everything inline
+    kFlushTailCall,     // one call for everything after the partial stores
+    kFlushLastCall      // no shortcut for an only contributor; counter inline; a call only
+                        // for the last contributor's combination
+};
+
+// Flush this warp's sums of squares of chunk k (rows 0..R-1) as one double partial per row,
+// then finish the chunk if this warp is its only or its last contributor. The warp works
+// range q (groups g0..g1, first chunk kfirst) as warp wir of wpr.
+template <int R, FlushCode CODE>
+__device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, int wir, int64_t k,
+                                            int64_t kfirst, int64_t g0, int64_t g1, Sum2 (&acc)[R],
+                                            double* part, unsigned* cnt, float* scale_out, int64_t C,
+                                            const float* rows, int64_t row_stride, int lane)
+{
+    const int64_t idx0 = (q * wpr + wir) * pt.J + (k - kfirst);     // row 0's slot
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
+        if (lane == 0) part[idx0 + (int64_t)r * pt.P * wpr * pt.J] = d;
+        acc[r].s = 0.0f;
+        acc[r].e = 0.0f;
+    }
+    const bool sole = wpr == 1 && k * pt.CG >= g0 && (k + 1) * pt.CG <= g1;
+    if (CODE == kFlushInline) {
+        flush_rest<R>(pt, wpr, k, sole, idx0, part, cnt, scale_out, C, rows, row_stride, lane);
+    } else if (CODE == kFlushTailCall) {
+        flush_rest_outlined<R>(pt, wpr, k, sole, idx0, part, cnt, scale_out, C, rows, row_stride, lane);
+    } else {
+        __threadfence();
+        unsigned last = 0;
+        if (lane == 0) {
+            int64_t lo, hi;
+            chunk_contributors(pt, k, lo, hi);
+            const unsigned prev = atomicAdd(cnt + k, 1u);
+            last = (prev == (unsigned)((hi - lo + 1) * wpr - 1)) ? 1u : 0u;
+        }
+        last = __shfl_sync(kFull, last, 0);
+        if (last) combine_chunk_outlined<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
     }
 }
 

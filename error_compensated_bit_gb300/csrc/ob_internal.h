@@ -41,7 +41,7 @@ struct WorkerArgs {
     uint32_t* wbits;        // [W][n/32]
     const float* s_prev;    // [W][nchunks] scales of the previous step
     float* s_next;          // [W][nchunks] scales of this step (written by the last contributor)
-    double* part;           // [W][P][warps per block][J] partial sums of squares
+    double* part;           // [W][P][warps per range][J] partial sums of squares
     unsigned* cnt;          // [nchunks] arrival counters (zero between launches)
     unsigned* status;       // status word (0 = fine; see ob_tma.cuh)
     FastDiv cg_div;         // division by the groups per chunk
@@ -49,6 +49,7 @@ struct WorkerArgs {
     int64_t n, C;
     float b1, c1;
     int stages;             // pipeline stages per warp (set by the launcher)
+    int interleave;         // 1: one range per block, warps interleaved; 0: one range per warp
 };
 
 // Launch shape of the worker kernel for one (W, gradient type).
@@ -79,10 +80,11 @@ struct UpdateArgs {
     const float* v;            // [n] frozen variance
     float* x;                  // [n]
     float* m;                  // [n] out
-    float* s_prev;             // [W][nchunks] <- s_next (block 0, after all readers finished)
+    float* s_prev;             // [W][nchunks] <- s_next (no reader of s_prev runs in this step's update)
     const float* s_next;
     float* t_prev;             // [nchunks] <- t_next
-    int64_t NG, CG, nscales_w, nchunks;
+    int64_t NG, CG;
+    int64_t nscales_w, nchunks; // scales to move (W*nchunks and nchunks, or 0 when k_scales moves them)
     FastDiv cg_div;            // division by the groups per chunk
     float lr, eps, wd;
 };
@@ -136,6 +138,7 @@ cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaS
 WorkerConfig worker_config(int W, int dtype, int smem_budget);
 cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_scales(const UpdateArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_warmup(int dtype, const WarmupArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_export(const ExportArgs& a, int grid, cudaStream_t s);

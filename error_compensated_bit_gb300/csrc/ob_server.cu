@@ -52,8 +52,10 @@ __device__ __forceinline__ uint64_t transpose8x8(uint64_t x)
 // a = (sum over w ascending of +-S_wk)/W;  e_s = yprev - T_prev*sign(yprev);  y = a + e_s;
 // bit = (y >= 0); ybuf = y; chunk sums of y^2 -> T_next.
 // Memory per element: W/8 (worker bits) + 4 + 4 (y) + 1/8 (server bits).
+// Register budgets (measured): up to 8 workers at 64 registers (four blocks per SM); beyond
+// that no residency request (0), which leaves the compiler its own choice.
 template <int W>
-__global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
+__global__ void __launch_bounds__(kBlock, (W > 8 ? 0 : 4)) k_server(ServerArgs a)
 {
     constexpr int T = W < 8 ? W : 8;     // workers covered by the table
     constexpr int U = W > 8 ? 2 : 1;     // groups per iteration
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
 
         for (int64_t gi = g0; gi < g1;) {
             if (gi == kend) {
-                flush_chunk<1, (W > 8)>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+                flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
                 ++k;
                 kend += pt.CG;
 #pragma unroll
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kBlock) k_server(ServerArgs a)
             }
             gi += nu;
         }
-        flush_chunk<1, (W > 8)>(pt, q, 1, 0, k, kfirst, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+        flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
 }
 
@@ -196,10 +198,21 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
         }
     }
 
+    // this step's scales become the previous ones (nothing in the update reads those); when
+    // they are many, k_scales does it instead and the counts here are zero
     if (blockIdx.x == 0) {
         for (int64_t i = threadIdx.x; i < a.nscales_w; i += blockDim.x) a.s_prev[i] = a.s_next[i];
         for (int64_t i = threadIdx.x; i < a.nchunks; i += blockDim.x) a.t_prev[i] = a.t_next[i];
     }
+}
+
+// This step's scales become the previous ones, over the whole grid (many scales).
+__global__ void __launch_bounds__(kBlock) k_scales(UpdateArgs a)
+{
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = tid; i < a.nscales_w; i += nthreads) a.s_prev[i] = a.s_next[i];
+    for (int64_t i = tid; i < a.nchunks; i += nthreads) a.t_prev[i] = a.t_next[i];
 }
 
 // Momentum mask (float 0/1) -> packed bits, bit = (mask != 0).
@@ -286,6 +299,12 @@ int occupancy_update()
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_update<false>, kBlock, 0) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_update<true>, kBlock, 0) != cudaSuccess) return 0;
     return b0 < b1 ? b0 : b1;
+}
+
+cudaError_t launch_scales(const UpdateArgs& a, int grid, cudaStream_t s)
+{
+    k_scales<<<grid, kBlock, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s)

@@ -107,13 +107,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
     const uint64_t pol = policy_evict_first();
     uint32_t phase = 0;   // bit s: parity of stage s's next completion
 
-    // Each block works one contiguous range of groups; its warps take the range's groups
-    // in turn (warp wib: groups g0 + wib, g0 + wib + wpb, ...), so the warps of a block
-    // stream neighbouring rows together.
-    for (int64_t q = blockIdx.x; q < pt.P; q += gridDim.x) {
+    // Interleaved mode (chunks much longer than a block's range): each block works one
+    // contiguous range of groups and its warps take the range's groups in turn (warp wib:
+    // g0 + wib, g0 + wib + wpb, ...), so the warps of a block stream neighbouring rows
+    // together. Otherwise (short chunks) each warp works its own contiguous range, so
+    // that no warp has to account for chunks it never touches.
+    const bool inter = a.interleave != 0;
+    const int wpr = inter ? wpb : 1;            // warps per range
+    const int wir = inter ? wib : 0;            // this warp's index within its range
+    const int64_t q0 = inter ? (int64_t)blockIdx.x : (int64_t)blockIdx.x * wpb + wib;
+    const int64_t qstep = inter ? (int64_t)gridDim.x : (int64_t)gridDim.x * wpb;
+    for (int64_t q = q0; q < pt.P; q += qstep) {
         const int64_t g0 = range_begin(pt, q);
         const int64_t g1 = range_begin(pt, q + 1);
-        const int64_t count = g1 - g0 > wib ? (g1 - g0 - wib + wpb - 1) / wpb : 0;
+        const int64_t count = g1 - g0 > wir ? (g1 - g0 - wir + wpr - 1) / wpr : 0;
         const int64_t items = count * NB;   // (group, row block) pairs, in order
         const int64_t klast = (g1 - 1) / pt.CG;
 
@@ -121,7 +128,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
         auto issue = [&](int s, int64_t it) {
             const uint32_t bar = bar0 + 8u * s;
             const uint32_t dst = st0 + (uint32_t)s * St::kBytes;
-            const int64_t e0 = (g0 + wib + (it / NB) * wpb) * 256;
+            const int64_t e0 = (g0 + wir + (it / NB) * wpr) * 256;
             const int b = (int)(it % NB);
             const int rows = (W - b * R) < R ? (W - b * R) : R;
             mbar_arrive_expect(bar, (uint32_t)rows * (St::kGradRow + St::kZRow) + (b == 0 ? 256u * 4u : 0u));
@@ -147,12 +154,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
             for (int64_t it = 0; it < S && it < items; ++it) issue((int)it, it);
 
         for (int64_t i = 0; i < count; ++i) {
-            const int64_t gi = g0 + wib + i * wpb;
+            const int64_t gi = g0 + wir + i * wpr;
             const int64_t kg = fast_div((uint32_t)gi, a.cg_div);
             if (kg != k) {
                 // this warp's part of chunks k .. kg-1 is done (possibly empty)
                 while (k < kg) {
-                    flush_chunk<W, true>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+                    flush_chunk<W, kFlushTailCall>(pt, q, wpr, wir, k, kfirst, g0, g1, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
                     ++k;
                 }
 #pragma unroll
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
             }
         }
         for (;;) {
-            flush_chunk<W, true>(pt, q, wpb, wib, k, kfirst, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+            flush_chunk<W, kFlushTailCall>(pt, q, wpr, wir, k, kfirst, g0, g1, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
             if (k == klast) break;
             ++k;
         }

@@ -17,11 +17,11 @@ OB_OK, OB_EINVAL, OB_ECUDA, OB_ENOTIMPL, OB_EALIGN, OB_ESCRATCH = 0, -1, -2, -3,
 OB_NOALLOC_SCRATCH_BYTES = 4 << 20
 OB_F32, OB_F16, OB_BF16 = 0, 1, 2
 (OB_K_WORKER, OB_K_SERVER, OB_K_UPDATE, OB_K_WARMUP, OB_K_LOCO_ABSMAX, OB_K_LOCO_QUANT,
- OB_K_LOCO_SERVER, OB_K_MASK, OB_K_EXPORT, OB_K_COUNT) = range(10)
+ OB_K_LOCO_SERVER, OB_K_MASK, OB_K_EXPORT, OB_K_SCALES, OB_K_COUNT) = range(11)
 KERNEL_NAMES = {OB_K_WORKER: "worker", OB_K_SERVER: "server", OB_K_UPDATE: "update",
                 OB_K_WARMUP: "warmup", OB_K_LOCO_ABSMAX: "loco_absmax",
                 OB_K_LOCO_QUANT: "loco_quant", OB_K_LOCO_SERVER: "loco_server",
-                OB_K_MASK: "mask", OB_K_EXPORT: "export"}
+                OB_K_MASK: "mask", OB_K_EXPORT: "export", OB_K_SCALES: "scales"}
 
 # Symbols the header declares, with their ctypes signatures.
 _vp, _i64, _i32, _f, _int, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,

@@ -78,11 +78,13 @@ enum {
 
 enum { OB_F32 = 0, OB_F16 = 1, OB_BF16 = 2 };   /* gradient storage formats */
 
-/* Kernel ids for ob_profile_read. */
+/* Kernel ids for ob_profile_read. OB_K_SCALES is the copy of a step's chunk scales into
+ * the "previous" slots; it runs as a kernel of its own only when the scales are many
+ * (short chunks), otherwise inside the update kernel. */
 enum {
     OB_K_WORKER = 0, OB_K_SERVER = 1, OB_K_UPDATE = 2, OB_K_WARMUP = 3,
     OB_K_LOCO_ABSMAX = 4, OB_K_LOCO_QUANT = 5, OB_K_LOCO_SERVER = 6,
-    OB_K_MASK = 7, OB_K_EXPORT = 8, OB_K_COUNT = 9
+    OB_K_MASK = 7, OB_K_EXPORT = 8, OB_K_SCALES = 9, OB_K_COUNT = 10
 };
 
 /* ---- context ------------------------------------------------------------------------ */
@@ -158,7 +160,9 @@ int ob_warmup_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m
  *   server:    a = (sum over w ascending of S_wk*sign_w)/W;  y = a + e_s;
  *              T_k = rms(y over chunk k);  send sign(y), T_k;  e_s = y - T_k*sign(y)
  *   all:       m = T_k*sign(y) [* mask];  x -= lr*(m/(sqrt(v)+eps) [+wd*x])
- * Three kernels on the stream: worker compress, server average/recompress, update.
+ * Three kernels on the stream: worker compress, server average/recompress, update; a
+ * fourth (OB_K_SCALES) moves the step's chunk scales into the "previous" slots when
+ * they are more than 4096 (short chunks), which the update does itself otherwise.
  */
 int ob_compressed_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m,
                        const float *v, float *worker_err, float *server_err, void *ws,

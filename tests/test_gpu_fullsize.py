@@ -18,13 +18,18 @@ from gpu_util import assert_close
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
+# (workload, W, phase, chunk): chunk None is the workload's own (n/W); the short chunks
+# run the worker with one range per warp, scales written by their only contributor and
+# the separate scale-copy kernel.
 CASES = [
-    ("bertL", 8, "compressed"),
-    ("bertB", 8, "compressed"),
-    ("sweep", 2, "compressed"),
-    ("sweep", 16, "compressed"),
-    ("loco", 4, "loco"),
-    ("loco", 4, "compressed"),
+    ("bertL", 8, "compressed", None),
+    ("bertL", 8, "compressed", 2048),
+    ("bertB", 8, "compressed", None),
+    ("sweep", 2, "compressed", None),
+    ("sweep", 16, "compressed", None),
+    ("sweep", 16, "compressed", 256),
+    ("loco", 4, "loco", None),
+    ("loco", 4, "compressed", None),
 ]
 
 
@@ -39,14 +44,15 @@ def _view(ws, ptr, count, dtype):
     return ws[off:off + count * size].view(dtype)
 
 
-@pytest.mark.parametrize("name,W,phase", CASES, ids=["%s-W%d-%s" % c for c in CASES])
-def test_full_size_sampled_chunks(ora, name, W, phase):
+@pytest.mark.parametrize("name,W,phase,chunk", CASES,
+                         ids=["%s-W%d-%s%s" % (c[:3] + ("" if c[3] is None else "-C%d" % c[3],)) for c in CASES])
+def test_full_size_sampled_chunks(ora, name, W, phase, chunk):
     from error_compensated_bit_gb300 import build, ob, synth
     if not torch.cuda.is_available():
         pytest.fail("needs a CUDA device")
     build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    wl = synth.workload(name, W=W)
+    wl = synth.workload(name, W=W, chunk=chunk)
     n, C = wl.n, wl.C
     nch = n // C
     ctx = ob.Context(n, W, C, wl.b1, wl.b2, wl.eps, wl.lr)
