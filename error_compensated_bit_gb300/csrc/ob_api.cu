@@ -9,6 +9,7 @@
 
 #include "../../include/ob.h"
 #include "ob_internal.h"
+#include "ob_tma.cuh"
 
 using namespace ob;
 
@@ -658,6 +659,18 @@ int ob_profile_read(ob_ctx* c, int kernel, double* total_ms, int64_t* launches)
 }
 
 int64_t ob_launch_count(const ob_ctx* c) { return c ? c->launches : -1; }
+
+int ob_selftest_wait(ob_ctx* c, void* ws, uint64_t limit_ns, void* stream)
+{
+    if (!c || limit_ns == 0 || limit_ns > kWaitLimitNs) return OB_EINVAL;
+    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (int r = check_device(c)) return r;
+    unsigned* status = at<unsigned>(ws, c->lay.status);
+    const cudaError_t e = launch_wait_probe(status, limit_ns, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->launches += 1;
+    return OB_OK;
+}
 
 int ob_read_status(ob_ctx* c, const void* ws, unsigned* status, void* stream)
 {

@@ -139,6 +139,7 @@ WorkerConfig worker_config(int W, int dtype, int smem_budget);
 cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_scales(const UpdateArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_warmup(int dtype, const WarmupArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_export(const ExportArgs& a, int grid, cudaStream_t s);

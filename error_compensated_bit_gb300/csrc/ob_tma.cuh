@@ -58,17 +58,22 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, at most kWaitLimitNs.
-// Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Wait for the phase with the given parity to complete, at most limit_ns (and at most
+// 2^30 polls). Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t spins = 0; spins < (1u << 30); ++spins) {
         if (mbar_test(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global to

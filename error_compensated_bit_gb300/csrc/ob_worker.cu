@@ -222,6 +222,28 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
     }
 }
 
+// Self-test of the failure path: one warp waits, with the given limit, on an mbarrier that
+// expects one arrival and never gets it; the wait runs out and the warp records the same
+// status the pipelines record. No copy is in flight, so returning is safe.
+__global__ void __launch_bounds__(32, 1) k_wait_probe(unsigned* status, uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    const bool landed = __all_sync(kFull, mbar_wait_for(b, 0u, limit_ns));
+    if (!landed && threadIdx.x == 0) atomicOr(status, kStatusWaitTimeout);
+}
+
+cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s)
+{
+    k_wait_probe<<<1, 32, 0, s>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 // Launch shape for (W, gradient type): warps per block and stages per warp chosen so that
 // the stages fill the shared memory of one block (one block per SM): at least two stages
 // per warp, up to sixteen warps, and as many stages as then fit (at most eight).

@@ -51,6 +51,7 @@ SIGNATURES = {
                                ctypes.POINTER(_i64)]),
     "ob_launch_count": (_i64, [_vp]),
     "ob_read_status": (_int, [_vp, _vp, ctypes.POINTER(ctypes.c_uint), _vp]),
+    "ob_selftest_wait": (_int, [_vp, _vp, ctypes.c_uint64, _vp]),
     "ob_strerror": (ctypes.c_char_p, [_int]),
     "ob_last_cuda_error": (_int, []),
     "ob_worker_compress_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -211,6 +212,10 @@ class Context:
         st = ctypes.c_uint()
         _call("ob_read_status", self.h, _ptr(ws), ctypes.byref(st), _stream(stream))
         return st.value
+
+    def selftest_wait(self, ws, limit_ns=1_000_000, stream=None):
+        """Enqueue a bounded wait that runs out (sets status 1 in the workspace)."""
+        _call("ob_selftest_wait", self.h, _ptr(ws), int(limit_ns), _stream(stream))
 
     def worker_compress_noalloc(self, grads, m, worker_err, scale_prev, wbits, scale_out,
                                 stream=None):

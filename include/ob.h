@@ -245,6 +245,16 @@ int64_t ob_launch_count(const ob_ctx *ctx);
  */
 int ob_read_status(ob_ctx *ctx, const void *ws, unsigned *status, void *stream);
 
+/*
+ * Self-test of the failure detection above (the pages have no counterpart). Enqueues one
+ * warp that waits, at most limit_ns nanoseconds (1 .. 2e9), on a shared-memory barrier
+ * that nothing completes -- the situation of a pipeline stage whose copy never lands.
+ * The wait runs out, the warp sets status 1 in the workspace's status word and returns;
+ * nothing is copied, nothing faults, and the device stays usable. Read the result with
+ * ob_read_status; ob_workspace_init clears it. OB_EINVAL for a limit outside the range.
+ */
+int ob_selftest_wait(ob_ctx *ctx, void *ws, uint64_t limit_ns, void *stream);
+
 /* Text for a status code; the last CUDA error number seen by this thread. */
 const char *ob_strerror(int code);
 int ob_last_cuda_error(void);

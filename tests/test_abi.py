@@ -108,6 +108,9 @@ def test_calls_reject_bad_arguments(ob):
     assert lib.ob_set_step(h, 41) == ob.OB_OK and lib.ob_get_step(h) == 41
     assert lib.ob_set_lr(h, float("inf")) == ob.OB_EINVAL
     assert lib.ob_profile_read(h, 99, None, None) == ob.OB_EINVAL
+    assert lib.ob_selftest_wait(h, ws, 0, S) == ob.OB_EINVAL
+    assert lib.ob_selftest_wait(h, ws, 3 * 10 ** 9, S) == ob.OB_EINVAL
+    assert lib.ob_selftest_wait(h, ws_odd, 1000, S) == ob.OB_EALIGN
     assert lib.ob_launch_count(h) == 0, "rejected calls launch nothing"
     lib.ob_destroy(h)
 
