@@ -184,11 +184,21 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
                 float mv[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    float mi = signed_scale(T[u], (sb[u] >> j) & 1u);
-                    if (masked) mi = __fmul_rn(mi, ((mb[u] >> j) & 1u) ? 1.0f : 0.0f);
-                    mv[j] = mi;
+                    const float st = signed_scale(T[u], (sb[u] >> j) & 1u);
                     const float denom = __fadd_rn(__fsqrt_rn(vv[u][j]), a.eps);
-                    float uu = __fdiv_rn(mi, denom);
+                    float mi = st, uu;
+                    if (masked) {
+                        // a masked element has mi = st*0 = +-0 and mi/denom = mi (denom > 0);
+                        // the quotient is formed from st and then selected, so the division
+                        // never sees the zero numerators that send it down its slow path
+                        const bool on = ((mb[u] >> j) & 1u) != 0u;
+                        mi = __fmul_rn(st, on ? 1.0f : 0.0f);
+                        const float q = __fdiv_rn(st, denom);
+                        uu = on ? q : mi;
+                    } else {
+                        uu = __fdiv_rn(mi, denom);
+                    }
+                    mv[j] = mi;
                     if (a.wd != 0.0f) uu = __fadd_rn(uu, __fmul_rn(a.wd, xv[u][j]));
                     xv[u][j] = __fsub_rn(xv[u][j], __fmul_rn(a.lr, uu));
                 }
