@@ -164,11 +164,11 @@ __global__ void __launch_bounds__(kBlock) k_loco_server(LocoArgs a)
         ld8_stream(a.x + e0, xv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float gbar = __fdiv_rn(acc[j], fW);
+            const float gbar = div_rn_zero_fast(acc[j], fW);
             mv[j] = __fadd_rn(__fmul_rn(a.b1, mv[j]), __fmul_rn(a.c1, gbar));
             vv[j] = __fadd_rn(__fmul_rn(a.b2, vv[j]), __fmul_rn(a.c2, __fmul_rn(gbar, gbar)));
             const float denom = __fadd_rn(__fsqrt_rn(vv[j]), a.eps);
-            float u = __fdiv_rn(mv[j], denom);
+            float u = div_rn_zero_fast(mv[j], denom);
             if (a.wd != 0.0f) u = __fadd_rn(u, __fmul_rn(a.wd, xv[j]));
             xv[j] = __fsub_rn(xv[j], __fmul_rn(a.lr, u));
         }
