@@ -560,7 +560,9 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     a.wd = c->wd;
     const cudaError_t e = cudaMemsetAsync(a.amax_bits, 0, (size_t)c->W * c->nchunks * 4, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int grid = stream_grid(c);
+    // four blocks per SM: one full wave of the server pass (four resident), and the
+    // quantize pass measured fastest with four of its five resident blocks
+    const int grid = c->sms * 4;
     if (int r = launch(c, OB_K_LOCO_ABSMAX, s, [&] { return launch_loco_absmax(dtype, a, grid, s); })) return r;
     if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_quant(dtype, a, grid, s); })) return r;
     if (int r = launch(c, OB_K_LOCO_SERVER, s, [&] { return launch_loco_server(a, grid, s); })) return r;
