@@ -131,17 +131,6 @@ __device__ __forceinline__ float signed_scale(float s, bool nonneg)
     return nonneg ? s : -s;
 }
 
-// x / d, bit-identical to __fdiv_rn(x, d). IEEE division takes a slow path for a zero
-// numerator, and zero numerators are common here (masked or never-touched elements,
-// averages of quantized zeros); for d > 0 the quotient of a zero is that zero (its sign
-// kept), so it is selected instead, and the division is given a nonzero numerator.
-__device__ __forceinline__ float div_rn_zero_fast(float x, float d)
-{
-    const bool zero = (x == 0.0f) & (d > 0.0f);
-    const float q = __fdiv_rn(zero ? 1.0f : x, d);
-    return zero ? x : q;
-}
-
 // ---- reductions --------------------------------------------------------------------------------
 
 // Error-free accumulation of squares in float32: every z^2 is split exactly into

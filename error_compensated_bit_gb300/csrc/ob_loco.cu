@@ -17,6 +17,7 @@
 // Memory per element: pass 1 W*(grad+4), pass 2 W*(grad+8+bits/8), pass 3
 // W*bits/8 + 24.
 #include "ob_common.cuh"
+#include "ob_div.cuh"
 
 namespace ob {
 

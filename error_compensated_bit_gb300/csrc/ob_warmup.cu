@@ -12,6 +12,7 @@
 //   x = x - lr*(mh/(sqrt(vh)+eps) [+ wd*x])
 // Memory per element: W*(grad bytes) + 24 (m, v, x read and written).
 #include "ob_common.cuh"
+#include "ob_div.cuh"
 
 namespace ob {
 
