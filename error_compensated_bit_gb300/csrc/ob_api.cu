@@ -251,7 +251,11 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
     int occ = c->device >= 0 ? occupancy_server(W) : 0;
     occ = pow2_floor(occ > 0 ? occ : 2);
     c->grid_s = c->sms * occ;
-    c->pts = make_part(n, chunk, (int64_t)c->grid_s * kWarpsPerBlock);
+    // one range per warp, but at least four groups per range: on small buffers fewer,
+    // longer ranges leave fewer partials to combine per chunk (measured faster)
+    const int64_t srv_ranges = (int64_t)c->grid_s * kWarpsPerBlock;
+    const int64_t srv_cap = (n / 256) / 4 > 0 ? (n / 256) / 4 : 1;
+    c->pts = make_part(n, chunk, srv_ranges < srv_cap ? srv_ranges : srv_cap);
     const int occ_u = c->device >= 0 ? occupancy_update() : 0;
     c->grid_u = c->sms * (occ_u > 0 ? occ_u : 2);
     c->lay = make_layout(n, W, c->nchunks, wpart, c->pts.P * c->pts.J);
