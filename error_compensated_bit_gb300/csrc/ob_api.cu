@@ -47,6 +47,8 @@ struct ob_ctx {
     Part pts{};                 // server partition
     int grid_s = 0;
     int grid_u = 0;             // update kernel: one resident wave
+    int loco_occ_a[3] = {};     // resident blocks per SM of the LoCo absmax / quantize
+    int loco_occ_q[3][2] = {};  // passes (per gradient type and code width; 0 = not asked)
     Layout lay{};
     bool has_mask = false;
     int64_t launches = 0;
@@ -564,11 +566,16 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     a.wd = c->wd;
     const cudaError_t e = cudaMemsetAsync(a.amax_bits, 0, (size_t)c->W * c->nchunks * 4, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    // four blocks per SM: one full wave of the server pass (four resident), and the
-    // quantize pass measured fastest with four of its five resident blocks
+    // the absmax and quantize passes: one resident wave, each warp a contiguous range;
+    // the server pass: four blocks per SM (its full wave), grid-stride
+    const int bi = bits == 4 ? 0 : 1;
+    if (!c->loco_occ_a[dtype]) c->loco_occ_a[dtype] = occupancy_loco_absmax(dtype);
+    if (!c->loco_occ_q[dtype][bi]) c->loco_occ_q[dtype][bi] = occupancy_loco_quant(dtype, bits);
+    const int grid_a = c->sms * (c->loco_occ_a[dtype] > 0 ? c->loco_occ_a[dtype] : 2);
+    const int grid_q = c->sms * (c->loco_occ_q[dtype][bi] > 0 ? c->loco_occ_q[dtype][bi] : 2);
     const int grid = c->sms * 4;
-    if (int r = launch(c, OB_K_LOCO_ABSMAX, s, [&] { return launch_loco_absmax(dtype, a, grid, s); })) return r;
-    if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_quant(dtype, a, grid, s); })) return r;
+    if (int r = launch(c, OB_K_LOCO_ABSMAX, s, [&] { return launch_loco_absmax(dtype, a, grid_a, s); })) return r;
+    if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_quant(dtype, a, grid_q, s); })) return r;
     if (int r = launch(c, OB_K_LOCO_SERVER, s, [&] { return launch_loco_server(a, grid, s); })) return r;
     c->step += 1;
     return OB_OK;

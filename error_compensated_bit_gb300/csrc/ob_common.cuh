@@ -106,6 +106,59 @@ struct Grad<__nv_bfloat16> {
     }
 };
 
+// The same loads split in two: raw() issues the 16- or 32-byte load and keeps the bits as
+// loaded (four registers for a 16-bit format), widen() converts them when they are used,
+// so that a kernel with several groups in flight holds the narrow form meanwhile.
+template <typename G>
+struct GradRaw {
+    uint4 r;
+    static __device__ __forceinline__ GradRaw load(const void* base, int64_t idx)
+    {
+        return GradRaw{__ldcs(reinterpret_cast<const uint4*>(static_cast<const G*>(base) + idx))};
+    }
+    __device__ __forceinline__ void widen(float (&v)[8]) const;
+};
+
+template <>
+struct GradRaw<float> {
+    float4 a, b;
+    static __device__ __forceinline__ GradRaw load(const void* base, int64_t idx)
+    {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
+        return GradRaw{__ldcs(p), __ldcs(p + 1)};
+    }
+    __device__ __forceinline__ void widen(float (&v)[8]) const
+    {
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+
+template <>
+__device__ __forceinline__ void GradRaw<__half>::widen(float (&v)[8]) const
+{
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h;
+        memcpy(&h, &w[i], 4);
+        const float2 f = __half22float2(h);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+template <>
+__device__ __forceinline__ void GradRaw<__nv_bfloat16>::widen(float (&v)[8]) const
+{
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 // ---- sign bits ---------------------------------------------------------------------------------
 
 // Lane `lane` holds the sign bits of elements 8*lane .. 8*lane+7 of a group in `byte`.

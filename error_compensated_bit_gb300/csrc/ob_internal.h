@@ -150,5 +150,7 @@ cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s);
 // Resident blocks per SM of the server kernel for W / of the update kernel; 0 on error.
 int occupancy_server(int W);
 int occupancy_update();
+int occupancy_loco_absmax(int dtype);
+int occupancy_loco_quant(int dtype, int bits);
 
 }  // namespace ob

@@ -28,96 +28,154 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// Work items are the W*n/256 groups of 256 elements of the [W][n] rows, numbered in
+// memory order (item t starts at element t*256 of the flat array; n is a multiple of the
+// chunk, so item t lies in scale slot t / (chunk/256) = w*nchunks + k). Each warp owns one
+// contiguous, balanced range of items (the grid is one resident wave) and keeps kLocoU
+// groups' loads in flight per iteration.
+constexpr int kLocoU = 4;
+
+__device__ __forceinline__ void warp_items(int64_t total, int64_t& t0, int64_t& t1)
+{
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    t0 = warp * total / nwarps;
+    t1 = (warp + 1) * total / nwarps;
+}
+
 template <typename G>
 __global__ void __launch_bounds__(kBlock) k_loco_absmax(LocoArgs a)
 {
+    constexpr int U = kLocoU;
     const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t groups = (int64_t)a.W * a.NG;      // row w's groups follow row w-1's
-    const int64_t CG = a.C / 256;
-    // Consecutive warps take consecutive groups (coalesced); each warp keeps a running
-    // max for the (row, chunk) it is in and publishes it only when that changes, so the
-    // few scale slots see one atomic per warp and chunk rather than one per group.
-    int64_t cur = -1;
+    int64_t t0, t1;
+    warp_items((int64_t)a.W * a.NG, t0, t1);
+    // the running max of the scale slot the warp is in, published (atomicMax on the float
+    // bits, exact and order-free) only when the slot changes
+    int64_t cur = t0 < t1 ? (int64_t)fast_div((uint32_t)t0, a.cg_div) : -1;
     float run = 0.0f;
-    for (int64_t t = warp; t < groups; t += nwarps) {
-        const int64_t w = fast_div((uint32_t)t, a.ng_div), gi = t - w * a.NG;
-        const int64_t key = w * a.nchunks + fast_div((uint32_t)gi, a.cg_div);
-        if (key != cur) {
-            const float mx = warp_max(run);
-            if (cur >= 0 && lane == 0) atomicMax(a.amax_bits + cur, __float_as_uint(mx));
-            cur = key;
-            run = 0.0f;
-        }
-        const int64_t e0 = gi * 256 + lane * 8;
-        float gv[8], ev[8];
-        Grad<G>::ld8(a.g, w * a.n + e0, gv);
-        ld8_stream(a.err + w * a.n + e0, ev);
+    for (int64_t tb = t0; tb < t1; tb += U) {
+        GradRaw<G> gr[U];
+        float ev[U][8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) run = fmaxf(run, fabsf(__fadd_rn(gv[j], ev[j])));
+        for (int u = 0; u < U; ++u) {
+            if (tb + u < t1) {
+                const int64_t e0 = (tb + u) * 256 + lane * 8;
+                gr[u] = GradRaw<G>::load(a.g, e0);
+                ld8_stream(a.err + e0, ev[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (tb + u < t1) {
+                const int64_t key = fast_div((uint32_t)(tb + u), a.cg_div);
+                if (key != cur) {
+                    const float mx = warp_max(run);
+                    if (lane == 0) atomicMax(a.amax_bits + cur, __float_as_uint(mx));
+                    cur = key;
+                    run = 0.0f;
+                }
+                float gv[8];
+                gr[u].widen(gv);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) run = fmaxf(run, fabsf(__fadd_rn(gv[j], ev[u][j])));
+            }
+        }
     }
-    const float mx = warp_max(run);
-    if (cur >= 0 && lane == 0) atomicMax(a.amax_bits + cur, __float_as_uint(mx));
+    if (cur >= 0) {
+        const float mx = warp_max(run);
+        if (lane == 0) atomicMax(a.amax_bits + cur, __float_as_uint(mx));
+    }
+}
+
+// Quantize one lane's 8 elements of a group with scale s (inv = rn(1/s)) and update the
+// moving average of the errors in place; returns the codes packed as stored.
+template <int BITS>
+__device__ __forceinline__ void quantize8(const float (&gv)[8], float (&ev)[8], float s, float inv,
+                                          float beta, float keep, uint32_t& lo, uint32_t& hi)
+{
+    const float L = (float)((1 << (BITS - 1)) - 1);
+    constexpr float kTieMargin = (float)(1 << (BITS - 1)) * 0x1p-21f;   // (L + 1) 2^-21
+    int qv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float c = __fadd_rn(gv[j], ev[j]);
+        int qi = 0;
+        if (s > 0.0f) {
+            // rint(c/s) with c/s correctly rounded, as defined. |c/s| <= L(1+u), and
+            // c * rn(1/s) lies within 3u|c/s| < (L+1) 2^-22 of rn(c/s); unless it is that
+            // close to a half-integer, both round to the same integer. Near a half-integer
+            // (the test keeps twice that distance) or when 1/s overflows, the quotient is
+            // formed exactly.
+            const float qq = __fmul_rn(c, inv);
+            float r = rintf(qq);
+            if (!(fabsf(__fsub_rn(qq, r)) < 0.5f - kTieMargin)) r = rintf(__fdiv_rn(c, s));
+            r = fminf(fmaxf(r, -L), L);
+            qi = (int)r;
+        }
+        qv[j] = qi;
+        const float e = __fsub_rn(c, __fmul_rn((float)qi, s));
+        ev[j] = __fadd_rn(__fmul_rn(beta, ev[j]), __fmul_rn(keep, e));
+    }
+    lo = 0;
+    hi = 0;
+    if (BITS == 4) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lo |= ((uint32_t)qv[j] & 0xfu) << (4 * j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            lo |= ((uint32_t)qv[j] & 0xffu) << (8 * j);
+            hi |= ((uint32_t)qv[j + 4] & 0xffu) << (8 * j);
+        }
+    }
 }
 
 template <typename G, int BITS>
 __global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
 {
+    constexpr int U = kLocoU;
     const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t groups = (int64_t)a.W * a.NG;
-    const int64_t CG = a.C / 256;
     const float L = (float)((1 << (BITS - 1)) - 1);
-    constexpr float kTieMargin = (float)(1 << (BITS - 1)) * 0x1p-21f;   // (L + 1) 2^-21
-    const int64_t row_bytes = a.n * BITS / 8;
-    for (int64_t t = warp; t < groups; t += nwarps) {
-        const int64_t w = fast_div((uint32_t)t, a.ng_div), gi = t - w * a.NG;
-        const int64_t k = fast_div((uint32_t)gi, a.cg_div);
-        const float s = __fdiv_rn(__uint_as_float(__ldcg(a.amax_bits + w * a.nchunks + k)), L);
-        const float inv = __frcp_rn(s);
-        if (lane == 0 && gi == k * CG) a.scale[w * a.nchunks + k] = s;
-        const int64_t e0 = gi * 256 + lane * 8;
-        float gv[8], ev[8];
-        Grad<G>::ld8(a.g, w * a.n + e0, gv);
-        ld8_stream(a.err + w * a.n + e0, ev);
-        int qv[8];
+    int64_t t0, t1;
+    warp_items((int64_t)a.W * a.NG, t0, t1);
+    const int64_t CG = a.C / 256;
+    // scale of the slot the warp is in, and its reciprocal; formed again only when the
+    // slot changes (a warp's range crosses one or two slots)
+    int64_t cur = -1;
+    float s = 0.0f, inv = 0.0f;
+    for (int64_t tb = t0; tb < t1; tb += U) {
+        GradRaw<G> gr[U];
+        float ev[U][8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float c = __fadd_rn(gv[j], ev[j]);
-            int qi = 0;
-            if (s > 0.0f) {
-                // rint(c/s) with c/s correctly rounded, as defined. |c/s| <= L(1+u), and
-                // c * rn(1/s) lies within 3u|c/s| < (L+1) 2^-22 of rn(c/s); unless it is
-                // that close to a half-integer, both round to the same integer. Near a
-                // half-integer (the test keeps twice that distance) or when 1/s overflows,
-                // the quotient is formed exactly.
-                const float qq = __fmul_rn(c, inv);
-                float r = rintf(qq);
-                if (!(fabsf(__fsub_rn(qq, r)) < 0.5f - kTieMargin)) r = rintf(__fdiv_rn(c, s));
-                r = fminf(fmaxf(r, -L), L);
-                qi = (int)r;
+        for (int u = 0; u < U; ++u) {
+            if (tb + u < t1) {
+                const int64_t e0 = (tb + u) * 256 + lane * 8;
+                gr[u] = GradRaw<G>::load(a.g, e0);
+                ld8_stream(a.err + e0, ev[u]);
             }
-            qv[j] = qi;
-            const float e = __fsub_rn(c, __fmul_rn((float)qi, s));
-            ev[j] = __fadd_rn(__fmul_rn(a.beta, ev[j]), __fmul_rn(a.keep, e));
         }
-        st8_stream(a.err + w * a.n + e0, ev);
-        uint8_t* out = a.codes + w * row_bytes + e0 * BITS / 8;
-        if (BITS == 4) {
-            uint32_t word = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) word |= ((uint32_t)qv[j] & 0xfu) << (4 * j);
-            __stcs(reinterpret_cast<unsigned int*>(out), word);
-        } else {
-            uint32_t lo = 0, hi = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                lo |= ((uint32_t)qv[j] & 0xffu) << (8 * j);
-                hi |= ((uint32_t)qv[j + 4] & 0xffu) << (8 * j);
+        for (int u = 0; u < U; ++u) {
+            const int64_t t = tb + u;
+            if (t < t1) {
+                const int64_t key = fast_div((uint32_t)t, a.cg_div);
+                if (key != cur) {
+                    cur = key;
+                    s = __fdiv_rn(__uint_as_float(__ldcg(a.amax_bits + key)), L);
+                    inv = __frcp_rn(s);
+                }
+                if (lane == 0 && t == key * CG) a.scale[key] = s;
+                float gv[8];
+                gr[u].widen(gv);
+                uint32_t lo, hi;
+                quantize8<BITS>(gv, ev[u], s, inv, a.beta, a.keep, lo, hi);
+                const int64_t e0 = t * 256 + lane * 8;
+                st8_stream(a.err + e0, ev[u]);
+                uint8_t* out = a.codes + e0 * BITS / 8;
+                if (BITS == 4) __stcs(reinterpret_cast<unsigned int*>(out), lo);
+                else __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
             }
-            __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
         }
     }
 }
@@ -199,6 +257,32 @@ cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream
         else k_loco_quant<__nv_bfloat16, 8><<<grid, kBlock, 0, s>>>(a);
     }
     return cudaGetLastError();
+}
+
+template <typename K>
+static int occ_of(K kernel)
+{
+    int blocks = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kBlock, 0) == cudaSuccess ? blocks : 0;
+}
+
+int occupancy_loco_absmax(int dtype)
+{
+    if (dtype == 0) return occ_of(k_loco_absmax<float>);
+    if (dtype == 1) return occ_of(k_loco_absmax<__half>);
+    return occ_of(k_loco_absmax<__nv_bfloat16>);
+}
+
+int occupancy_loco_quant(int dtype, int bits)
+{
+    if (bits == 4) {
+        if (dtype == 0) return occ_of(k_loco_quant<float, 4>);
+        if (dtype == 1) return occ_of(k_loco_quant<__half, 4>);
+        return occ_of(k_loco_quant<__nv_bfloat16, 4>);
+    }
+    if (dtype == 0) return occ_of(k_loco_quant<float, 8>);
+    if (dtype == 1) return occ_of(k_loco_quant<__half, 8>);
+    return occ_of(k_loco_quant<__nv_bfloat16, 8>);
 }
 
 cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s)

@@ -221,12 +221,15 @@ def test_warmup_then_compressed(ora):
             tr.compare(t, gpu.snapshot(), out, st, check_mask=mask)
 
 
-@pytest.mark.parametrize("W,dtype,bits", [(4, "bf16", 4), (2, "f32", 8), (3, "f16", 4)])
-def test_loco_parity(ora, W, dtype, bits):
+@pytest.mark.parametrize("W,dtype,bits,per_row", [(4, "bf16", 4, 2), (2, "f32", 8, 2), (3, "f16", 4, 2),
+                                                   (4, "bf16", 4, 400), (2, "f32", 8, 25)])
+def test_loco_parity(ora, W, dtype, bits, per_row):
+    """per_row chunks per worker row: 400 makes every 256-element group a chunk of its
+    own, so a warp's range crosses many scale slots."""
     from error_compensated_bit_gb300 import ob
-    rng = np.random.default_rng(40 + W)
+    rng = np.random.default_rng(40 + W + per_row)
     n = W * 256 * 400
-    C = n // W // 2
+    C = n // W // per_row
     st = random_state(rng, n, W, C)
     st.v[:] = 0.0
     gpu = CudaPath(st)
