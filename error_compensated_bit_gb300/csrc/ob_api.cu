@@ -191,6 +191,10 @@ Part make_part(int64_t n, int64_t chunk, int64_t want)
 
 bool finite(float v) { return std::isfinite(v); }
 
+// The no-allocation path's scratch array (defined at the end of this file).
+constexpr size_t kNoallocStatusOff = OB_NOALLOC_SCRATCH_BYTES - 256;   // its status word
+int noalloc_scratch(int dev, void** out);
+
 }  // namespace
 
 extern "C" {
@@ -231,6 +235,16 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
         c->device = -1;
         c->sms = 152;
         c->smem_budget = 232448;
+    }
+    // the worker kernels' shared-memory opt-in is a per-context property of the device:
+    // set here, for this device, so contexts on several devices (and host threads) each
+    // have it without a process-wide flag
+    if (c->device >= 0) {
+        const cudaError_t e = prepare_worker(W, c->smem_budget);
+        if (e != cudaSuccess) {
+            delete c;
+            return cuda_fail(e);
+        }
     }
     // worker: one block per SM, one range per block
     int64_t wpart = 0;
@@ -676,9 +690,17 @@ int64_t ob_launch_count(const ob_ctx* c) { return c ? c->launches : -1; }
 int ob_selftest_wait(ob_ctx* c, void* ws, uint64_t limit_ns, void* stream)
 {
     if (!c || limit_ns == 0 || limit_ns > kWaitLimitNs) return OB_EINVAL;
-    if (int r = check_ptr(ws, kAlignWs)) return r;
+    if (ws != nullptr)
+        if (int r = check_ptr(ws, kAlignWs)) return r;
     if (int r = check_device(c)) return r;
-    unsigned* status = at<unsigned>(ws, c->lay.status);
+    unsigned* status = nullptr;
+    if (ws != nullptr) {
+        status = at<unsigned>(ws, c->lay.status);
+    } else {
+        void* scratch = nullptr;    // the no-allocation path's status word
+        if (int r = noalloc_scratch(c->device, &scratch)) return r;
+        status = at<unsigned>(scratch, kNoallocStatusOff);
+    }
     const cudaError_t e = launch_wait_probe(status, limit_ns, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
     c->launches += 1;
@@ -717,63 +739,124 @@ int ob_last_cuda_error(void) { return g_last_cuda; }
 
 // ---- worker pass without any allocation ------------------------------------------------------
 //
-// For callers that cannot allocate device memory (inside a stream capture, or behind a
-// runtime that owns all device memory): the worker kernel's scratch -- per-range partial
-// sums and per-chunk arrival counters -- lives in this fixed array instead of a
-// caller-provided workspace. Every GPU that loads the library holds the array until the
-// process exits. Host code may not use the array's name as an address: it only stands
-// for the symbol there, so the device address is looked up once per device, with that
-// device current, by cudaGetSymbolAddress.
+// For callers that cannot allocate device memory themselves (a runtime that hands out
+// every byte of device memory from its own arena, or a caller with no allocator at
+// all): the worker kernel's scratch -- per-range partial sums and per-chunk arrival
+// counters -- lives in this fixed array instead of a caller-provided workspace. Every
+// GPU that loads the library holds the array until the process exits. Its last 256
+// bytes hold a status word that only ob_noalloc_read_status clears.
+//
+// Host code may not use the array's name as an address: it only stands for the symbol
+// there. The device address is looked up with cudaGetSymbolAddress, with the device
+// current, the first time a context of the driver is seen on that device, and again if
+// that context changes (a device reset unloads the module, which may come back at
+// another address).
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[OB_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on `dev` (which must be current); looked up on the
-// first call for that device and remembered.
+struct NoallocSlot {
+    unsigned long long ctx_id = 0;   // driver context the address belongs to (0: none yet)
+    void* addr = nullptr;
+};
+
+std::mutex g_noalloc_mu;
+NoallocSlot g_noalloc[kMaxDevices];
+
+// The current driver context's unique id (never reused within a process), through the
+// driver's entry points as the runtime exposes them; 0 if unavailable.
+unsigned long long current_context_id()
+{
+    using GetCurrent = int (*)(void**);
+    using GetId = int (*)(void*, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        cudaGetLastError();
+    });
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+    return id;
+}
+
+// Device address of the scratch array on `dev` (which must be current).
 int noalloc_scratch(int dev, void** out)
 {
     if (dev < 0 || dev >= kMaxDevices) return OB_EINVAL;
+    // id 0: no context is current on this thread yet; the lookup below makes the
+    // device's primary context current, and the id is taken again after it
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    NoallocSlot& slot = g_noalloc[dev];
+    if (!slot.addr || id == 0 || slot.ctx_id != id) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
-        g_noalloc_addr[dev] = p;
+        slot.addr = p;
+        slot.ctx_id = id != 0 ? id : current_context_id();
     }
-    *out = g_noalloc_addr[dev];
+    *out = slot.addr;
     return OB_OK;
+}
+
+// [p, p + bytes) and [q, q + qbytes) share a byte.
+bool overlap(const void* p, size_t bytes, const void* q, size_t qbytes)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + qbytes && b < a + bytes;
 }
 
 }  // namespace
 
-extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtype, const float* m,
-                                          float* worker_err, const float* scale_prev, uint32_t* wbits,
-                                          float* scale_out, void* stream)
+extern "C" {
+
+int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtype, const float* m, float* worker_err,
+                               const float* scale_prev, uint32_t* wbits, float* scale_out, void* stream)
 {
     if (!c) return OB_EINVAL;
     if (int r = check_grads(c, grads, dtype)) return r;
     for (const void* p : {(const void*)m, (const void*)worker_err, (const void*)scale_prev,
                           (const void*)wbits, (const void*)scale_out})
         if (int r = check_ptr(p, 16)) return r;
-    if (scale_prev == scale_out) return OB_EINVAL;
-    // scratch: partial sums [W][P][warps per range][J] doubles, then one counter per chunk
+    // every output is disjoint from every other buffer (worker_err is updated in place)
+    const size_t Wn = (size_t)c->W * (size_t)c->n;
+    const size_t sc_bytes = (size_t)c->W * (size_t)c->nchunks * 4;
+    struct Buf {
+        const void* p;
+        size_t bytes;
+    };
+    const Buf bufs[] = {{grads, Wn * grad_bytes(dtype)}, {m, (size_t)c->n * 4}, {worker_err, Wn * 4},
+                        {scale_prev, sc_bytes}, {wbits, Wn / 8}, {scale_out, sc_bytes}};
+    for (int o : {2, 4, 5})
+        for (int i = 0; i < 6; ++i)
+            if (i != o && overlap(bufs[o].p, bufs[o].bytes, bufs[i].p, bufs[i].bytes)) return OB_EINVAL;
+    // scratch: partial sums [W][P][warps per range][J] doubles, then one counter per chunk;
+    // the status word sits apart, in the array's last 256 bytes
     const Part& pt = c->ptw[dtype];
     const size_t part_bytes = up((size_t)c->W * pt.P * c->wpr[dtype] * pt.J * 8, kAlignWs);
     const size_t cnt_bytes = up((size_t)c->nchunks * 4, 16);
-    if (part_bytes + cnt_bytes + 16 > (size_t)OB_NOALLOC_SCRATCH_BYTES) return OB_ESCRATCH;
+    if (part_bytes + cnt_bytes > kNoallocStatusOff) return OB_ESCRATCH;
     if (int r = check_device(c)) return r;
     void* scratch = nullptr;
     if (int r = noalloc_scratch(c->device, &scratch)) return r;
     const cudaStream_t s = (cudaStream_t)stream;
     unsigned* cnt = at<unsigned>(scratch, part_bytes);
-    // the counters (and the status word after them) must start at zero; the partials are
-    // written before they are read
-    const cudaError_t e = cudaMemsetAsync(cnt, 0, cnt_bytes + 16, s);
+    // the counters must start at zero; the partials are written before they are read
+    const cudaError_t e = cudaMemsetAsync(cnt, 0, cnt_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e);
 
     WorkerArgs wa{};
@@ -785,7 +868,7 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
     wa.s_next = scale_out;
     wa.part = at<double>(scratch, 0);
     wa.cnt = cnt;
-    wa.status = at<unsigned>(scratch, part_bytes + cnt_bytes);
+    wa.status = at<unsigned>(scratch, kNoallocStatusOff);
     wa.pt = pt;
     wa.interleave = c->wpr[dtype] > 1 ? 1 : 0;
     wa.cg_div = make_fastdiv((uint32_t)(c->C / 256));
@@ -796,3 +879,20 @@ extern "C" int ob_worker_compress_noalloc(ob_ctx* c, const void* grads, int dtyp
     const int grid_w = c->sms;
     return launch(c, OB_K_WORKER, s, [&] { return launch_worker(c->W, dtype, wa, grid_w, s, c->smem_budget); });
 }
+
+int ob_noalloc_read_status(ob_ctx* c, unsigned* status, void* stream)
+{
+    if (!c || !status) return OB_EINVAL;
+    if (int r = check_device(c)) return r;
+    void* scratch = nullptr;
+    if (int r = noalloc_scratch(c->device, &scratch)) return r;
+    const cudaStream_t s = (cudaStream_t)stream;
+    unsigned* word = at<unsigned>(scratch, kNoallocStatusOff);
+    cudaError_t e = cudaMemcpyAsync(status, word, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(word, 0, 4, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return OB_OK;
+}
+
+}  // extern "C"

@@ -136,6 +136,8 @@ struct LocoArgs {
 constexpr int kBlock = 256;
 cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaStream_t s, int smem_budget);
 WorkerConfig worker_config(int W, int dtype, int smem_budget);
+// Opt the worker kernels for W into their dynamic shared memory on the current device.
+cudaError_t prepare_worker(int W, int smem_budget);
 cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_scales(const UpdateArgs& a, int grid, cudaStream_t s);

@@ -269,17 +269,30 @@ static cudaError_t launch_wg(const WorkerArgs& a, int grid, cudaStream_t s, int 
 {
     const WorkerConfig c = config_w<W, G>(smem_budget);
     if ((int)c.smem_bytes > smem_budget) return cudaErrorInvalidConfiguration;
-    static bool attr_set = false;   // per instantiation; the budget does not change per process
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(k_worker<W, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)c.smem_bytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     WorkerArgs b = a;
     b.stages = c.stages;
     k_worker<W, G><<<grid, c.warps_per_block * 32, c.smem_bytes, s>>>(b);
     return cudaGetLastError();
+}
+
+// The shared-memory opt-in of the worker kernels for W, on the current device. It is a
+// property of the kernel in the current device's context, so it is set for every context
+// (see prepare_worker), not once per process.
+template <int W, typename G>
+static cudaError_t prepare_wg(int smem_budget)
+{
+    const WorkerConfig c = config_w<W, G>(smem_budget);
+    if ((int)c.smem_bytes > smem_budget) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(k_worker<W, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem_bytes);
+}
+
+template <int W>
+static cudaError_t prepare_w(int smem_budget)
+{
+    cudaError_t e = prepare_wg<W, float>(smem_budget);
+    if (e == cudaSuccess) e = prepare_wg<W, __half>(smem_budget);
+    if (e == cudaSuccess) e = prepare_wg<W, __nv_bfloat16>(smem_budget);
+    return e;
 }
 
 template <int W>
@@ -306,6 +319,18 @@ cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaS
 #define OB_CASE(w) \
     case w:        \
         return launch_w<w>(dtype, a, grid, s, smem_budget);
+        OB_FOR_EACH_W(OB_CASE)
+#undef OB_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_worker(int W, int smem_budget)
+{
+    switch (W) {
+#define OB_CASE(w) \
+    case w:        \
+        return prepare_w<w>(smem_budget);
         OB_FOR_EACH_W(OB_CASE)
 #undef OB_CASE
     }

@@ -55,6 +55,7 @@ SIGNATURES = {
     "ob_strerror": (ctypes.c_char_p, [_int]),
     "ob_last_cuda_error": (_int, []),
     "ob_worker_compress_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ob_noalloc_read_status": (_int, [_vp, ctypes.POINTER(ctypes.c_uint), _vp]),
 }
 
 _LIB = None
@@ -214,7 +215,8 @@ class Context:
         return st.value
 
     def selftest_wait(self, ws, limit_ns=1_000_000, stream=None):
-        """Enqueue a bounded wait that runs out (sets status 1 in the workspace)."""
+        """Enqueue a bounded wait that runs out (sets status 1 in the workspace; with
+        ws None, in the no-allocation worker pass's status word)."""
         _call("ob_selftest_wait", self.h, _ptr(ws), int(limit_ns), _stream(stream))
 
     def worker_compress_noalloc(self, grads, m, worker_err, scale_prev, wbits, scale_out,
@@ -222,3 +224,9 @@ class Context:
         """The worker pass with its scratch in the library's fixed array (no workspace)."""
         _call("ob_worker_compress_noalloc", self.h, _ptr(grads), dtype_code(grads), _ptr(m),
               _ptr(worker_err), _ptr(scale_prev), _ptr(wbits), _ptr(scale_out), _stream(stream))
+
+    def noalloc_read_status(self, stream=None):
+        """Synchronize, return and clear the no-allocation worker pass's status word."""
+        st = ctypes.c_uint()
+        _call("ob_noalloc_read_status", self.h, ctypes.byref(st), _stream(stream))
+        return st.value

@@ -93,8 +93,11 @@ enum {
  * Create a context for an n-element buffer, W workers and `chunk` elements per scale,
  * with Adam's b1, b2, eps and the learning rate lr (weight decay 0, bias correction
  * off, as in the tutorial page's BERT configurations, §6.2). Queries the current
- * device; allocates host memory only. Returns OB_EINVAL for sizes outside the rules
- * above or non-finite hyper-parameters; *out is set only on OB_OK.
+ * device and, when there is one, opts the worker kernels into the dynamic shared memory
+ * they launch with on that device (OB_ECUDA if that fails); allocates host memory only.
+ * Contexts on different devices, or used from different host threads, are independent.
+ * Returns OB_EINVAL for sizes outside the rules above or non-finite hyper-parameters;
+ * *out is set only on OB_OK.
  */
 int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, float lr,
             ob_ctx **out);
@@ -251,7 +254,9 @@ int ob_read_status(ob_ctx *ctx, const void *ws, unsigned *status, void *stream);
  * that nothing completes -- the situation of a pipeline stage whose copy never lands.
  * The wait runs out, the warp sets status 1 in the workspace's status word and returns;
  * nothing is copied, nothing faults, and the device stays usable. Read the result with
- * ob_read_status; ob_workspace_init clears it. OB_EINVAL for a limit outside the range.
+ * ob_read_status; ob_workspace_init clears it. With ws == NULL the warp sets the status
+ * word of the no-allocation worker pass instead (read with ob_noalloc_read_status).
+ * OB_EINVAL for a limit outside the range.
  */
 int ob_selftest_wait(ob_ctx *ctx, void *ws, uint64_t limit_ns, void *stream);
 
@@ -262,10 +267,10 @@ int ob_last_cuda_error(void);
 /* ---- a worker pass that allocates nothing ------------------------------------------------ */
 
 /*
- * For callers that cannot allocate device memory at all -- code that runs while a
- * stream is being captured into a CUDA graph (where cudaMalloc is not allowed), or a
- * host runtime that hands out every byte of device memory from its own arena and has
- * no room for a separate workspace.
+ * For callers that cannot allocate device memory themselves: a host runtime that
+ * reserves all device memory up front and hands it out from its own arena (with no room
+ * left for a separate workspace), or an embedding in which the caller has no device
+ * allocator at all, only buffers that someone else owns.
  *
  * The pages have no counterpart of this entry point: it is a packaging of the worker
  * pass of ob_compressed_step (momentum, error compensation, sign packing and chunk
@@ -285,20 +290,30 @@ int ob_last_cuda_error(void);
  *                at the top of this file)
  *   scale_prev   [W][n/chunk] scales of the previous step (input; zeros at the start)
  *   wbits        [W][n/32] packed signs               (output)
- *   scale_out    [W][n/chunk] this step's scales      (output; must not alias scale_prev)
+ *   scale_out    [W][n/chunk] this step's scales      (output)
+ * An output that shares any byte with another of these buffers is rejected (OB_EINVAL).
  *
  * The scratch array is shared by every call in the process: calls whose kernels could
  * run at the same time on the GPU (different streams, or different host threads) race
  * on it and must be serialized by the caller. Each call clears the counters it needs
  * before its kernel runs; the rest of the array keeps whatever the last call left.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current, so make that first call before any
- * stream capture begins.
+ *
+ * The device address of the array is looked up (cudaGetSymbolAddress) by the first call
+ * on each device, with that device current, and again whenever the device's context has
+ * changed since (after a device reset the library's module may be loaded at another
+ * address). Make that first call before any stream capture begins.
+ *
+ * Failures: a bounded pipeline wait that runs out (see ob_read_status) leaves this
+ * call's outputs invalid and sets a status word kept in the array's last 256 bytes,
+ * which no call clears. ob_noalloc_read_status synchronizes the stream, reports the word
+ * (0: every such call since the last read finished normally; 1: a wait ran out) and
+ * clears it.
  */
 #define OB_NOALLOC_SCRATCH_BYTES (4u << 20)
 int ob_worker_compress_noalloc(ob_ctx *ctx, const void *grads, int dtype, const float *m,
                                float *worker_err, const float *scale_prev, uint32_t *wbits,
                                float *scale_out, void *stream);
+int ob_noalloc_read_status(ob_ctx *ctx, unsigned *status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -255,6 +255,57 @@ def test_loco_parity(ora, W, dtype, bits, per_row):
     assert np.array_equal(err_d.cpu().numpy(), err), "LoCo has no sums: bit-exact"
 
 
+def test_contexts_in_host_threads(ora):
+    """Two contexts created and driven from two host threads at once, each on its own
+    stream (the worker kernels' shared-memory opt-in is set per context, not through a
+    process-wide flag): both match the oracle."""
+    import threading
+    cases = [(4, "f16", 61), (8, "bf16", 62)]
+    setups, results, errors = [], {}, []
+    for W, dtype, seed in cases:
+        rng = np.random.default_rng(seed)
+        n = W * 256 * 96
+        st = random_state(rng, n, W, n // W // 2)
+        grads = [_grads(rng, W, n, dtype) for _ in range(3)]
+        setups.append((W, st, grads))
+    # the oracle's results first, on copies of the initial states
+    starts = [st.copy() for _, st, _ in setups]
+    want = []
+    for W, st, grads in setups:
+        outs = [ora.compressed_step(st, g) for g in grads]
+        want.append((outs[-1], st))
+    barrier = threading.Barrier(len(setups))
+
+    def run(i):
+        try:
+            W, _, grads = setups[i]
+            gpu = CudaPath(starts[i])
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            from gpu_util import to_device_grads
+            gd = [to_device_grads(g, "cuda") for g in grads]
+            torch.cuda.synchronize()
+            barrier.wait()
+            for g in gd:
+                gpu.ctx.compressed_step(g, gpu.x, gpu.m, gpu.v, gpu.ew, gpu.es, gpu.ws, side)
+            side.synchronize()
+            results[i] = gpu.snapshot()
+        except Exception as e:         # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(len(setups))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i, (out, st) in enumerate(want):
+        got = results[i]
+        assert np.array_equal(got["sbits"], out["sbits"]), "context %d server signs" % i
+        assert_close("context %d params" % i, got["x"], st.x)
+        assert_close("context %d momentum" % i, got["m"], st.m)
+
+
 def test_stream_ordering():
     """Calls are asynchronous on the given stream: a step enqueued on a side stream is
     ordered after work already on that stream and visible after synchronizing it."""
