@@ -13,8 +13,15 @@ Printed: one JSON line (rank 0) with the metric in params*workers/s, the step ti
 HBM roofline fraction of the dominant kernel (the worker pass) from CUDA events recorded
 by the library on its launch stream during the timed region, the end-to-end rate through
 the host-buffer entry point (gradients copied from pinned host memory every step, the
-server's compressed message copied back), sampled SM clocks, and the CPU oracle timed on
-a bounded sample of the same workload.
+server's compressed message copied back) beside the same copy timed alone, sampled SM
+clocks, and the CPU oracle timed on a bounded sample of the same workload. Every timed
+loop cycles through three seeded per-step gradient draws made before timing starts.
+
+With the default headline, a "workloads" object follows with the same measurements for
+every other workload of the recipe, run one after another with memory freed between
+them: the BERT-Base-sized step (masked, after its warm-up steps) and its warm-up step,
+the 2^28-element sweep at W = 2, 4, 8, 16 (compressed and warm-up steps), the GPT-like
+buffer's LoCo step and 1-bit step, and the tiny buffer (eager and from a CUDA graph).
 
 With --gpus N > 1 (launched by torchrun) every rank runs an independent replica on its
 own GPU (the path does not shard: the W workers already live on one GPU); the value is
@@ -56,6 +63,10 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--graph", action="store_true",
                    help="time replays of one step captured in a CUDA graph (small, launch-bound buffers)")
+    p.add_argument("--workloads", default="default",
+                   help="after the headline line's own workload, also time the other workloads: "
+                        "'default' (only when the headline is the default bertL step), 'all', 'none', "
+                        "or comma-separated substrings of their keys (e.g. 'sweep_W16,loco')")
     return p.parse_args()
 
 
@@ -257,6 +268,255 @@ def workload_desc(wl, phase):
 
 # ---- the GPU arm ----------------------------------------------------------------------
 
+KERNEL_OF_PHASE = {"compressed": "worker", "warmup": "warmup", "loco": "loco_quant"}
+GRAD_BUFFERS = 3        # per-step gradient draws, cycled through in every timed loop
+
+
+def dominant_kernel_bytes(phase, n, W, s_g):
+    """Algorithmic bytes of one launch of the phase's dominant kernel."""
+    if phase == "compressed":
+        return n * worker_bytes_per_elem(W, s_g)
+    if phase == "warmup":
+        return n * (W * s_g + 24.0)
+    return n * W * (s_g + 8.5)                     # LoCo quantize: g, e read; e, codes written
+
+
+class Run:
+    """One workload's device state, set up, warmed and timed through the C ABI.
+
+    Gradients for GRAD_BUFFERS steps (the recipe's seeded per-step draws) are drawn on the
+    device before anything is timed, and step t uses draw t mod GRAD_BUFFERS."""
+
+    def __init__(self, torch, ob, synth, dev, wl, phase):
+        self.torch, self.ob, self.synth, self.dev, self.wl, self.phase = torch, ob, synth, dev, wl, phase
+        n, W, C = wl.n, wl.W, wl.C
+        self.masked = wl.zero_frac > 0 and phase == "compressed"
+        self.ctx = ob.Context(n, W, C, wl.b1, wl.b2, wl.eps, wl.lr)
+        self.x = synth.params(wl, dev)
+        self.v = synth.variance(wl, dev)
+        self.m = torch.zeros(n, dtype=torch.float32, device=dev)
+        self.ew = torch.zeros(W, n, dtype=torch.float32, device=dev)
+        self.es = torch.zeros(n, dtype=torch.float32, device=dev)
+        self.ws = torch.empty(self.ctx.workspace_bytes(), dtype=torch.uint8, device=dev)
+        self.ctx.workspace_init(self.ws)
+        self.lws = None
+        if phase == "loco":
+            self.lws = torch.zeros(self.ctx.loco_workspace_bytes(4), dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        # the BERT-Base recipe runs its warm-up Adam steps before the compressed ones
+        self.grads = [synth.grads(wl, 1000 + t, dev) for t in range(GRAD_BUFFERS)]
+        if phase == "compressed" and wl.warmup_steps:
+            for t in range(wl.warmup_steps):
+                self.ctx.warmup_step(self.grads[t % GRAD_BUFFERS], self.x, self.m, self.v, self.ws, self.stream)
+        self.grads = [synth.grads(wl, t, dev, out=self.grads[t]) for t in range(GRAD_BUFFERS)]
+        if self.masked:
+            self.ctx.set_mask(synth.mask(wl, dev), self.ws)
+        self.t = 0
+
+    def step(self, stream=None):
+        s = stream or self.stream
+        g = self.grads[self.t % GRAD_BUFFERS]
+        self.t += 1
+        if self.phase == "compressed":
+            self.ctx.compressed_step(g, self.x, self.m, self.v, self.ew, self.es, self.ws, s)
+        elif self.phase == "warmup":
+            self.ctx.warmup_step(g, self.x, self.m, self.v, self.ws, s)
+        else:
+            self.ctx.loco_step(g, self.x, self.m, self.v, self.ew, self.lws, 0.9, 4, s)
+
+    def bytes_per_step(self):
+        return self.wl.n * bytes_per_elem(self.phase, self.wl.W, self.wl.grad_bytes, self.masked)
+
+    def measure(self, steps, warmup, graph=False, clocks=None, barrier_fn=None):
+        """Warm up, then time `steps` steps with CUDA events on the launch stream."""
+        torch, dev, ctx = self.torch, self.dev, self.ctx
+        for _ in range(max(3, warmup)):
+            self.step()
+        torch.cuda.synchronize(dev)
+        cuda_graph = None
+        graph_launches = 0
+        if graph:
+            # one captured graph per gradient buffer, replayed in turn
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(self.stream)
+            cuda_graph = []
+            for b in range(GRAD_BUFFERS):
+                gr = torch.cuda.CUDAGraph()
+                cap0 = ctx.launch_count()
+                with torch.cuda.graph(gr, stream=side):
+                    self.t = b
+                    self.step(torch.cuda.current_stream(dev))
+                graph_launches = ctx.launch_count() - cap0
+                cuda_graph.append(gr)
+            for gr in cuda_graph:
+                gr.replay()
+            torch.cuda.synchronize(dev)
+        b_step = self.bytes_per_step()
+        # a step that streams less than 8x the L2 could be served partly from it: then the
+        # L2 is flushed (a 2x-L2 buffer written) before every step, outside per-step events
+        flush = b_step < 8 * L2_BYTES
+        scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps if flush else 1)]
+        launches0 = ctx.launch_count()
+        ctx.profile(True)
+        if barrier_fn:
+            barrier_fn()
+        torch.cuda.synchronize(dev)
+        if clocks:
+            clocks.start()
+            time.sleep(0.3)
+        s = self.stream
+        if not flush:
+            ev[0][0].record(s)
+        for t in range(steps):
+            if flush:
+                scratch.fill_(float(t))
+                ev[t][0].record(s)
+            if cuda_graph is not None:
+                cuda_graph[t % GRAD_BUFFERS].replay()
+            else:
+                self.step()
+            if flush:
+                ev[t][1].record(s)
+        if not flush:
+            ev[0][1].record(s)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop() if clocks else None
+        if barrier_fn:
+            barrier_fn()
+        ms_total = sum(a.elapsed_time(b) for a, b in ev)
+        launches = ctx.launch_count() - launches0
+        if cuda_graph is not None:   # replays launch the captured kernels without the library's counter
+            launches = steps * graph_launches
+        per_kernel = {}
+        for k, name in self.ob.KERNEL_NAMES.items():
+            t_ms, cnt = ctx.profile_read(k)
+            if cnt:
+                per_kernel[name] = {"launches": cnt, "avg_us": 1e3 * t_ms / cnt, "share": t_ms / ms_total}
+        ctx.profile(False)
+        del scratch
+        dom = KERNEL_OF_PHASE[self.phase]
+        k_bytes = dominant_kernel_bytes(self.phase, self.wl.n, self.wl.W, self.wl.grad_bytes)
+        k_avg_us = per_kernel[dom]["avg_us"] if dom in per_kernel else None
+        return {"ms_total": ms_total, "steps": steps, "b_step": b_step, "flush": flush,
+                "kernels": per_kernel, "launches": launches, "clocks": clk,
+                "cuda_graph": cuda_graph is not None, "dominant": dom, "k_bytes": k_bytes,
+                "k_avg_us": k_avg_us}
+
+    def free(self):
+        for name in ("x", "v", "m", "ew", "es", "ws", "lws", "grads"):
+            setattr(self, name, None)
+        self.ctx.close()
+        self.torch.cuda.synchronize(self.dev)
+        self.torch.cuda.empty_cache()
+
+
+def summarize(run, res, peak):
+    """One workload's entry: step time, rate, the step's algorithmic GB/s against the peak,
+    the dominant kernel's roofline and every kernel's share of the step."""
+    wl = run.wl
+    ms_step = res["ms_total"] / res["steps"]
+    gbs = res["b_step"] / (ms_step / 1e3) / 1e9
+    dom = None
+    if res["k_avg_us"]:
+        ach = res["k_bytes"] / (res["k_avg_us"] / 1e6) / 1e9
+        dom = {"kernel": res["dominant"], "avg_us": res["k_avg_us"], "achieved_gbs": ach,
+               "frac": ach / peak, "algorithmic_bytes_per_launch": res["k_bytes"]}
+    return {"workload": workload_desc(wl, run.phase), "n": wl.n, "W": wl.W, "chunk": wl.C,
+            "grad_dtype": str(wl.grad_dtype).split(".")[-1], "masked": run.masked,
+            "steps": res["steps"], "ms_per_step": ms_step, "value": wl.n * wl.W / (ms_step / 1e3),
+            "unit": UNIT, "hbm_gbs_step": gbs, "hbm_frac_step": gbs / peak,
+            "bytes_per_step": res["b_step"], "dominant": dom,
+            "kernels": {k: {"avg_us": v["avg_us"], "share": v["share"]} for k, v in res["kernels"].items()},
+            "cuda_graph": res["cuda_graph"], "l2": "flushed before every step" if res["flush"] else "streamed (step >> L2)",
+            "gpu_launches": res["launches"], "clocks": res["clocks"]}
+
+
+# The workloads other than the headline, run in sequence after it (memory freed between):
+# (name, phase, workers or None for the recipe's, replayed from a CUDA graph)
+EXTRA_WORKLOADS = [
+    ("bertB", "compressed", None, False), ("bertB", "warmup", None, False),
+    ("sweep", "compressed", 2, False), ("sweep", "warmup", 2, False),
+    ("sweep", "compressed", 4, False), ("sweep", "warmup", 4, False),
+    ("sweep", "compressed", 8, False), ("sweep", "warmup", 8, False),
+    ("sweep", "compressed", 16, False), ("sweep", "warmup", 16, False),
+    ("loco", "loco", None, False), ("loco", "compressed", None, False),
+    ("tiny", "compressed", None, False), ("tiny", "compressed", None, True),
+]
+
+
+def run_extra_workloads(torch, ob, synth, dev, steps, warmup, peak, only=None):
+    out = {}
+    for name, phase, W, graph in EXTRA_WORKLOADS:
+        key = "%s%s_%s%s" % (name, "_W%d" % W if W else "", phase, "_graph" if graph else "")
+        if only and not any(o in key for o in only):
+            continue
+        wl = synth.workload(name, W=W)
+        run = Run(torch, ob, synth, dev, wl, phase)
+        n_steps = max(steps, 50) if name == "tiny" else steps
+        res = run.measure(n_steps, warmup, graph=graph, clocks=ClockSampler(_gpu_index(dev)))
+        out[key] = summarize(run, res, peak)
+        run.free()
+        del run
+    return out
+
+
+def _gpu_index(dev):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    return vis.split(",")[dev.index] if vis else dev.index
+
+
+def e2e_leg(torch, run, steps, dist, world):
+    """End to end through ob_compressed_step_host, plus the same host-to-device copy alone."""
+    wl, dev, ctx, stream = run.wl, run.dev, run.ctx, run.stream
+    n, W, C = wl.n, wl.W, wl.C
+    g0 = run.grads[0]
+    g_host = torch.empty(g0.shape, dtype=g0.dtype, pin_memory=True)
+    g_host.copy_(g0)
+    sb_host = torch.empty(n // 32, dtype=torch.int32, pin_memory=True)
+    ss_host = torch.empty(n // C, dtype=torch.float32, pin_memory=True)
+    # two device gradient buffers, alternated, so that the next step's host copy overlaps
+    # this step's kernels (the library orders each copy after the last worker pass that
+    # read the buffer); the timed draws are released to make room
+    g_dev = [run.grads[0], run.grads[1]]
+    run.grads = g_dev
+    x, m, v, ew, es, ws = run.x, run.m, run.v, run.ew, run.es, run.ws
+    for i in range(2):
+        ctx.compressed_step_host(g_host, g_dev[i % 2], x, m, v, ew, es, ws, sb_host, ss_host, stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        ctx.compressed_step_host(g_host, g_dev[i % 2], x, m, v, ew, es, ws, sb_host, ss_host, stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3)
+    h2d = int(g_host.numel() * g_host.element_size())
+    # the copy alone: the same pinned bytes, host to device, back to back on one stream
+    side = torch.cuda.Stream(dev)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        g_dev[0].copy_(g_host, non_blocking=True)
+        c0.record(side)
+        for i in range(steps):
+            g_dev[i % 2].copy_(g_host, non_blocking=True)
+        c1.record(side)
+    side.synchronize()
+    copy_ms = c0.elapsed_time(c1) / steps
+    out = {"value": n * W * steps * world / (e_ms / 1e3), "unit": UNIT,
+           "ms_per_step": e_ms / steps,
+           "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": int(n // 8 + (n // C) * 4),
+           "copy_only": {"ms_per_step": copy_ms, "h2d_gbs": h2d / (copy_ms / 1e3) / 1e9,
+                         "what": "the same pinned host-to-device gradient copy alone, back to back, "
+                                 "CUDA events on its stream: the link bound of the end-to-end step"},
+           "path": "ob_compressed_step_host each step: pinned host grads -> device (library copy "
+                   "stream, overlapped with the previous step's kernels), the step, server "
+                   "signs+scales -> pinned host; host wall clock with device syncs at both ends"}
+    del g_host, sb_host, ss_host
+    return out
+
+
 def gpu_arm(args, wl):
     import torch
     from error_compensated_bit_gb300 import build, ob, synth
@@ -268,180 +528,61 @@ def gpu_arm(args, wl):
     torch.cuda.set_device(dev)
     build.build()
     ob.load()
-
-    n, W, C = wl.n, wl.W, wl.C
-    s_g = wl.grad_bytes
-    masked = wl.zero_frac > 0 and args.phase == "compressed"
-    ctx = ob.Context(n, W, C, wl.b1, wl.b2, wl.eps, wl.lr)
-    x = synth.params(wl, dev)
-    v = synth.variance(wl, dev)
-    m = torch.zeros(n, dtype=torch.float32, device=dev)
-    ew = torch.zeros(W, n, dtype=torch.float32, device=dev)
-    es = torch.zeros(n, dtype=torch.float32, device=dev)
-    ws = torch.empty(ctx.workspace_bytes(), dtype=torch.uint8, device=dev)
-    ctx.workspace_init(ws)
-    g = synth.grads(wl, 0, dev)
-    mask = None
-    if masked:
-        mask = synth.mask(wl, dev)
-        ctx.set_mask(mask, ws)
-    lws = None
-    if args.phase == "loco":
-        lws = torch.zeros(ctx.loco_workspace_bytes(4), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def one_step():
-        if args.phase == "compressed":
-            ctx.compressed_step(g, x, m, v, ew, es, ws, stream)
-        elif args.phase == "warmup":
-            ctx.warmup_step(g, x, m, v, ws, stream)
-        else:
-            ctx.loco_step(g, x, m, v, ew, lws, 0.9, 4, stream)
-
-    # the BERT-Base recipe runs its warm-up steps before the compressed ones
-    if args.phase == "compressed" and wl.warmup_steps:
-        for t in range(wl.warmup_steps):
-            ctx.warmup_step(synth.grads(wl, t + 1, dev, out=g), x, m, v, ws, stream)
-        synth.grads(wl, 0, dev, out=g)
-    for _ in range(max(3, args.warmup)):
-        one_step()
-    torch.cuda.synchronize(dev)
-    graph = None
-    if args.graph:
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        cap0 = ctx.launch_count()
-        with torch.cuda.graph(graph, stream=side):
-            cap = torch.cuda.current_stream(dev)
-            if args.phase == "compressed":
-                ctx.compressed_step(g, x, m, v, ew, es, ws, cap)
-            elif args.phase == "warmup":
-                ctx.warmup_step(g, x, m, v, ws, cap)
-            else:
-                ctx.loco_step(g, x, m, v, ew, lws, 0.9, 4, cap)
-        graph_launches = ctx.launch_count() - cap0     # kernels captured per step
-        graph.replay()
-        torch.cuda.synchronize(dev)
-
-    # timed region
-    clocks = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                          os.environ["CUDA_VISIBLE_DEVICES"].split(",")[dev.index])
-    # A step that streams less than 8x the L2 could be served partly from it: then the L2
-    # is flushed (a 2x-L2 buffer written) before every step, outside per-step events.
-    b_step = n * bytes_per_elem(args.phase, W, s_g, masked)
-    flush = b_step < 8 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps if flush else 1)]
-    launches0 = ctx.launch_count()
-    ctx.profile(True)
-    barrier(dist)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.3)
-    if not flush:
-        ev[0][0].record(stream)
-    for t in range(args.steps):
-        if flush:
-            scratch.fill_(float(t))
-            ev[t][0].record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            one_step()
-        if flush:
-            ev[t][1].record(stream)
-    if not flush:
-        ev[0][1].record(stream)
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    barrier(dist)
-    ms_total = sum(a.elapsed_time(b) for a, b in ev)
-    launches = ctx.launch_count() - launches0
-    if graph is not None:     # replays launch the captured kernels without the library's counter
-        launches = args.steps * graph_launches
-    kid = {"compressed": ob.OB_K_WORKER, "warmup": ob.OB_K_WARMUP, "loco": ob.OB_K_LOCO_QUANT}[args.phase]
-    k_ms, k_n = ctx.profile_read(kid)
-    per_kernel = {}
-    for k, name in ob.KERNEL_NAMES.items():
-        t_ms, cnt = ctx.profile_read(k)
-        if cnt:
-            per_kernel[name] = {"launches": cnt, "avg_us": 1e3 * t_ms / cnt,
-                                "share": t_ms / ms_total}
-    ctx.profile(False)
-    ms_total = max_over_ranks(dist, ms_total)
-
-    ms_step = ms_total / args.steps
-    units = n * W * args.steps * world
-    value = units / (ms_total / 1e3)
     peak, peak_kind = load_peaks()
+
+    run = Run(torch, ob, synth, dev, wl, args.phase)
+    res = run.measure(args.steps, args.warmup, graph=args.graph, clocks=ClockSampler(_gpu_index(dev)),
+                      barrier_fn=lambda: barrier(dist))
+    n, W, C = wl.n, wl.W, wl.C
+    ms_total = max_over_ranks(dist, res["ms_total"])
+    ms_step = ms_total / args.steps
+    value = n * W * args.steps * world / (ms_total / 1e3)
+    b_step = res["b_step"]
+    k_avg_s = res["k_avg_us"] / 1e6 if res["k_avg_us"] else None
+    achieved = res["k_bytes"] / k_avg_s / 1e9 if k_avg_s else None
     if args.phase == "compressed":
-        k_bytes = n * worker_bytes_per_elem(W, s_g)
         khash = kernel_source_hash(["ob_worker.cu", "ob_common.cuh", "ob_tma.cuh"])
     elif args.phase == "warmup":
-        k_bytes = n * (W * s_g + 24.0)
         khash = kernel_source_hash(["ob_warmup.cu", "ob_common.cuh"])
     else:
-        k_bytes = n * W * (s_g + 8.5)
         khash = kernel_source_hash(["ob_loco.cu", "ob_common.cuh"])
-    # per-kernel events exist only for direct launches (not for graph replays)
-    k_avg_s = (k_ms / k_n) / 1e3 if k_n else None
-    achieved = k_bytes / k_avg_s / 1e9 if k_avg_s else None
     traffic = load_traffic(wl.name, W, khash) if args.phase == "compressed" else None
 
-    # end to end through the host-buffer entry point (compressed phase only)
     e2e = None
     if args.phase == "compressed" and args.e2e_steps > 0:
-        g_host = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
-        g_host.copy_(g)
-        sb_host = torch.empty(n // 32, dtype=torch.int32, pin_memory=True)
-        ss_host = torch.empty(n // C, dtype=torch.float32, pin_memory=True)
-        # two device gradient buffers, alternated, so that the next step's host copy
-        # overlaps this step's kernels (the library orders each copy after the last
-        # worker pass that read the buffer)
-        g_dev = [torch.empty_like(g), torch.empty_like(g)]
-        del g
-        for i in range(2):
-            ctx.compressed_step_host(g_host, g_dev[i % 2], x, m, v, ew, es, ws, sb_host, ss_host, stream)
-        torch.cuda.synchronize(dev)
-        barrier(dist)
-        t0 = time.perf_counter()
-        for i in range(args.e2e_steps):
-            ctx.compressed_step_host(g_host, g_dev[i % 2], x, m, v, ew, es, ws, sb_host, ss_host, stream)
-        torch.cuda.synchronize(dev)
-        e_ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3)
-        e2e = {"value": n * W * args.e2e_steps * world / (e_ms / 1e3), "unit": UNIT,
-               "ms_per_step": e_ms / args.e2e_steps,
-               "h2d_bytes_per_step": int(g_host.numel() * g_host.element_size()),
-               "d2h_bytes_per_step": int(n // 8 + (n // C) * 4),
-               "path": "ob_compressed_step_host each step: pinned host grads -> device (library copy "
-                       "stream, overlapped with the previous step's kernels), the step, server "
-                       "signs+scales -> pinned host; host wall clock with device syncs at both ends"}
-        del g_host, g_dev
+        e2e = e2e_leg(torch, run, args.e2e_steps, dist, world)
+    run.free()
+    del run
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(wl, args.phase), "n": n, "W": W, "chunk": C,
-                   "grad_dtype": str(wl.grad_dtype).split(".")[-1], "masked": masked,
-                   "cuda_graph": graph is not None,
+                   "grad_dtype": str(wl.grad_dtype).split(".")[-1], "masked": wl.zero_frac > 0 and args.phase == "compressed",
+                   "cuda_graph": res["cuda_graph"], "grad_buffers": GRAD_BUFFERS,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": ("flushed: a %d MB buffer written before every step, steps timed one by one "
                           "(each streams %.2f GB, under 8x the 129 MB L2)" % (2 * L2_BYTES // 10**6, b_step / 1e9)
-                          if flush else
+                          if res["flush"] else
                           "no flush: each step streams %.1f GB, far more than the 129 MB L2" % (b_step / 1e9))},
         "hbm_gbs_step": b_step / (ms_step / 1e3) / 1e9,
         "hbm_frac_step": b_step / (ms_step / 1e3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None, "traffic": traffic,
-                     "kernel": {"compressed": "worker", "warmup": "warmup", "loco": "loco_quant"}[args.phase],
-                     "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_avg_s * 1e6 if k_avg_s else None,
+                     "kernel": res["dominant"],
+                     "algorithmic_bytes_per_launch": res["k_bytes"], "avg_launch_us": res["k_avg_us"],
                      "peak_kind": "%s hbm_gbs (STREAM-style copy)" % peak_kind},
-        "kernels": per_kernel,
-        "clocks": clk, "gpu_launches": launches, "e2e": e2e,
+        "kernels": res["kernels"],
+        "clocks": res["clocks"], "gpu_launches": res["launches"], "e2e": e2e,
     }
+    default_run = args.workload == "bertL" and args.phase == "compressed" and args.n is None and args.chunk is None
+    if args.workloads != "none" and (default_run or args.workloads != "default"):
+        if world == 1:
+            only = None if args.workloads in ("default", "all") else args.workloads.split(",")
+            line["workloads"] = run_extra_workloads(torch, ob, synth, dev, args.steps, args.warmup, peak, only)
+        else:
+            line["workloads"] = "run at N=1 only (replicas add nothing per GPU)"
     if rank == 0 and not args.no_cpu_baseline:
         n_s = wl.W * 256 * 4096
         per, steps, u, desc = oracle_sample_run(wl, args.phase, n_s, args.cpu_seconds)

@@ -65,3 +65,21 @@ def test_worker_bytes_and_bertl_launch(bench):
     assert bench.worker_bytes_per_elem(8, 2) == 8 * (2 + 8 + 0.125) + 4 == 85.0
     n = 333_496_320
     assert n * bench.worker_bytes_per_elem(8, 2) == 28_347_187_200
+
+
+def test_dominant_kernel_bytes(bench):
+    # the roofline's kernel per phase: worker pass; the warm-up kernel (the whole warm-up
+    # step); LoCo quantize (gradient and error read, error and 4-bit code written per row)
+    n = 1_315_723_264
+    assert bench.dominant_kernel_bytes("compressed", n, 4, 2) == n * (4 * (2 + 8.125) + 4)
+    assert bench.dominant_kernel_bytes("warmup", n, 4, 2) == n * (4 * 2 + 24)
+    assert bench.dominant_kernel_bytes("loco", n, 4, 2) == n * 4 * (2 + 4 + 4 + 0.5)
+
+
+def test_extra_workloads_cover_every_recipe(bench):
+    keys = {(name, phase, W) for name, phase, W, _ in bench.EXTRA_WORKLOADS}
+    assert ("bertB", "compressed", None) in keys
+    for W in (2, 4, 8, 16):
+        assert ("sweep", "compressed", W) in keys and ("sweep", "warmup", W) in keys
+    assert ("loco", "loco", None) in keys and ("loco", "compressed", None) in keys
+    assert ("tiny", "compressed", None) in keys
