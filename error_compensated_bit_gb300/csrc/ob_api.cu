@@ -240,7 +240,8 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
     // set here, for this device, so contexts on several devices (and host threads) each
     // have it without a process-wide flag
     if (c->device >= 0) {
-        const cudaError_t e = prepare_worker(W, c->smem_budget);
+        cudaError_t e = prepare_worker(W, c->smem_budget);
+        if (e == cudaSuccess) e = prepare_server(W);
         if (e != cudaSuccess) {
             delete c;
             return cuda_fail(e);

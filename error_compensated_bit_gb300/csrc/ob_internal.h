@@ -136,8 +136,10 @@ struct LocoArgs {
 constexpr int kBlock = 256;
 cudaError_t launch_worker(int W, int dtype, const WorkerArgs& a, int grid, cudaStream_t s, int smem_budget);
 WorkerConfig worker_config(int W, int dtype, int smem_budget);
-// Opt the worker kernels for W into their dynamic shared memory on the current device.
+// Opt the worker / server kernels for W into their dynamic shared memory on the current
+// device (a property of the kernel in that device's context).
 cudaError_t prepare_worker(int W, int smem_budget);
+cudaError_t prepare_server(int W);
 cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_scales(const UpdateArgs& a, int grid, cudaStream_t s);

@@ -10,6 +10,7 @@
 // elements, every worker's packed words (the all-to-all), and the update pass reads
 // the server's words (the all-gather). Nothing is copied.
 #include "ob_common.cuh"
+#include "ob_tma.cuh"
 
 namespace ob {
 
@@ -52,10 +53,11 @@ __device__ __forceinline__ uint64_t transpose8x8(uint64_t x)
 // a = (sum over w ascending of +-S_wk)/W;  e_s = yprev - T_prev*sign(yprev);  y = a + e_s;
 // bit = (y >= 0); ybuf = y; chunk sums of y^2 -> T_next.
 // Memory per element: W/8 (worker bits) + 4 + 4 (y) + 1/8 (server bits).
-// Register budgets (measured): up to 8 workers at 64 registers (four blocks per SM); beyond
-// that no residency request (0), which leaves the compiler its own choice.
+// Used for W <= 8: one group's loads per warp in flight, 64 registers (four blocks per SM).
+// Keeping several groups in flight through shared memory (k_server_staged) measured slower
+// here, where the pass is close to bound by instruction issue; it pays for W > 8.
 template <int W>
-__global__ void __launch_bounds__(kBlock, (W > 8 ? 0 : 4)) k_server(ServerArgs a)
+__global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
 {
     constexpr int T = W < 8 ? W : 8;     // workers covered by the table
     constexpr int U = W > 8 ? 2 : 1;     // groups per iteration
@@ -139,6 +141,132 @@ __global__ void __launch_bounds__(kBlock, (W > 8 ? 0 : 4)) k_server(ServerArgs a
             }
             gi += nu;
         }
+        flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+    }
+}
+
+// The same pass for W > 8, where the per-element work grows and one group in flight per
+// warp no longer covers the memory latency. Each warp works one contiguous range of groups through a ring of kServerStages(W)
+// shared-memory stages: a stage holds one group's previous y (1 KB) and the group's 32
+// bytes of sign words from each worker row, copied by per-lane 16-byte asynchronous copies
+// (two per lane for y, one per lane for the first 2W lanes for the signs), so that several
+// groups' loads are in flight per warp without holding registers. Dynamic shared memory:
+// the warps' average tables, then the warps' rings.
+template <int W>
+struct ServerStage {
+    static constexpr int kStages = W > 8 ? 3 : 4;
+    static constexpr uint32_t kSignOff = 1024;                    // after the 256 y values
+    static constexpr uint32_t kBytes = 1024 + 32 * W;
+    static constexpr uint32_t kTabBytes = 4u << (W < 8 ? W : 8);  // one table per warp
+    static constexpr size_t kSmem = (size_t)(kBlock / 32) * (kTabBytes + kStages * kBytes);
+};
+
+template <int W>
+__global__ void __launch_bounds__(kBlock, 4) k_server_staged(ServerArgs a)
+{
+    using St = ServerStage<W>;
+    constexpr int T = W < 8 ? W : 8;     // workers covered by the table
+    constexpr int S = St::kStages;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    float* tab = reinterpret_cast<float*>(smem + (size_t)wib * St::kTabBytes);
+    unsigned char* ring = smem + (size_t)(kBlock / 32) * St::kTabBytes + (size_t)wib * S * St::kBytes;
+    const uint32_t ring_u32 = smem_u32(ring);
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const Part pt = a.pt;
+    const int64_t words_per_row = a.n / 32;
+    const uint64_t pol = policy_evict_first();
+
+    // this lane's copies of group gi into stage s: two 16-byte pieces of y, and piece
+    // (lane & 1) of worker row (lane >> 1)'s 32 bytes of sign words
+    auto issue = [&](int s, int64_t gi) {
+        const uint32_t dst = ring_u32 + (uint32_t)s * St::kBytes;
+        const float* ysrc = a.ybuf + gi * 256 + lane * 8;
+        cp_async16(dst + lane * 32, ysrc, pol);
+        cp_async16(dst + lane * 32 + 16, ysrc + 4, pol);
+        if (lane < 2 * W) {
+            const uint32_t* wsrc = a.wbits + (int64_t)(lane >> 1) * words_per_row + gi * 8 + (lane & 1) * 4;
+            cp_async16(dst + St::kSignOff + lane * 16, wsrc, pol);
+        }
+    };
+
+    for (int64_t q = warp; q < pt.P; q += nwarps) {
+        const int64_t g0 = range_begin(pt, q);
+        const int64_t g1 = range_begin(pt, q + 1);
+        int64_t k = g0 / pt.CG;
+        const int64_t kfirst = k;
+        int64_t kend = (k + 1) * pt.CG;
+
+        __syncwarp();                       // the previous range's last stage is read
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            if (g0 + s < g1) issue(s, g0 + s);
+            cp_async_commit();
+        }
+        float sw[W];
+#pragma unroll
+        for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
+        float tp = __ldg(a.t_prev + k);
+        build_average_table<W>(tab, sw, lane);
+        Sum2 acc[1] = {{0.0f, 0.0f}};
+
+        for (int64_t gi = g0; gi < g1; ++gi) {
+            if (gi == kend) {
+                flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+                ++k;
+                kend += pt.CG;
+#pragma unroll
+                for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
+                tp = __ldg(a.t_prev + k);
+                build_average_table<W>(tab, sw, lane);
+            }
+            const int s = (int)((gi - g0) % S);
+            cp_async_wait<S - 1>();         // this lane's copies of group gi have landed
+            __syncwarp();                   // ... and every other lane's
+            const unsigned char* stg = ring + (size_t)s * St::kBytes;
+            float yv[8];
+            {
+                const float4 y0 = reinterpret_cast<const float4*>(stg)[2 * lane];
+                const float4 y1 = reinterpret_cast<const float4*>(stg)[2 * lane + 1];
+                yv[0] = y0.x; yv[1] = y0.y; yv[2] = y0.z; yv[3] = y0.w;
+                yv[4] = y1.x; yv[5] = y1.y; yv[6] = y1.z; yv[7] = y1.w;
+            }
+            // byte (lane & 3) of word (lane >> 2) of each row: this lane's 8 sign bits
+            uint64_t lo = 0, hi = 0;
+#pragma unroll
+            for (int w = 0; w < T; ++w) lo |= (uint64_t)stg[St::kSignOff + w * 32 + lane] << (8 * w);
+            if (W > 8) {
+#pragma unroll
+                for (int w = 8; w < W; ++w) hi |= (uint64_t)stg[St::kSignOff + w * 32 + lane] << (8 * (w - 8));
+            }
+            __syncwarp();                   // every lane is done with stage s
+            if (gi + S < g1) issue(s, gi + S);
+            cp_async_commit();
+            lo = transpose8x8(lo);
+            if (W > 8) hi = transpose8x8(hi);
+            uint32_t byte = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float avg = tab[(uint32_t)(lo >> (8 * j)) & 0xffu];
+                if (W > 8) {
+                    const uint32_t pat = (uint32_t)(hi >> (8 * j)) & 0xffu;
+#pragma unroll
+                    for (int w = 8; w < W; ++w) avg = __fadd_rn(avg, signed_scale(sw[w], (pat >> (w - 8)) & 1u));
+                    avg = (W & (W - 1)) == 0 ? __fmul_rn(avg, 1.0f / (float)W) : __fdiv_rn(avg, (float)W);
+                }
+                const float es = __fsub_rn(yv[j], signed_scale(tp, yv[j] >= 0.0f));
+                const float y = __fadd_rn(avg, es);
+                yv[j] = y;
+                byte |= (y >= 0.0f ? 1u : 0u) << j;
+                sum2_add_sq(acc[0], y);
+            }
+            st8_stream(a.ybuf + gi * 256 + lane * 8, yv);
+            const uint32_t word = quad_word(byte, lane);
+            if ((lane & 3) == 0) __stcs(a.sbits + gi * 8 + (lane >> 2), word);
+        }
+        cp_async_wait<0>();                 // nothing of this range is left in flight
         flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
 }
@@ -258,16 +386,30 @@ __global__ void __launch_bounds__(kBlock) k_export(ExportArgs a)
 template <int W>
 static cudaError_t launch_s(const ServerArgs& a, int grid, cudaStream_t s)
 {
-    k_server<W><<<grid, kBlock, 0, s>>>(a);
+    if constexpr (W > 8) k_server_staged<W><<<grid, kBlock, ServerStage<W>::kSmem, s>>>(a);
+    else k_server<W><<<grid, kBlock, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+template <int W>
+static cudaError_t prepare_s()
+{
+    if constexpr (W <= 8) return cudaSuccess;
+    else return cudaFuncSetAttribute(k_server_staged<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)ServerStage<W>::kSmem);
 }
 
 template <int W>
 static int occ_s()
 {
     int blocks = 0;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_server<W>, kBlock, 0) == cudaSuccess
-               ? blocks : 0;
+    if (prepare_s<W>() != cudaSuccess) return 0;
+    cudaError_t e;
+    if constexpr (W > 8)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_server_staged<W>, kBlock, ServerStage<W>::kSmem);
+    else
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_server<W>, kBlock, 0);
+    return e == cudaSuccess ? blocks : 0;
 }
 
 #define OB_FOR_EACH_W(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) X(16)
@@ -278,6 +420,18 @@ cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s)
 #define OB_CASE(w) \
     case w:        \
         return launch_s<w>(a, grid, s);
+        OB_FOR_EACH_W(OB_CASE)
+#undef OB_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_server(int W)
+{
+    switch (W) {
+#define OB_CASE(w) \
+    case w:        \
+        return prepare_s<w>();
         OB_FOR_EACH_W(OB_CASE)
 #undef OB_CASE
     }

@@ -104,4 +104,27 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, ui
         : "memory");
 }
 
+// Per-thread asynchronous copies of 16 bytes from global to shared memory (both addresses
+// 16-byte aligned), grouped by commit and awaited by count: a copy lands in shared memory
+// without passing through registers, so a warp can keep several stages in flight at no
+// register cost. The wait is a hardware wait for this thread's own copies (no polling);
+// other lanes see the data after a __syncwarp.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 }  // namespace ob
