@@ -67,7 +67,7 @@ class Oracle:
             _i64, _i32, _f, _f, _f, _f, _f, _f, _f, _vp, ctypes.c_int, _f32p, _f32p, _f32p]
         lib.ora_warmup_step.restype = ctypes.c_int
         lib.ora_loco_step.argtypes = [
-            _i64, _i32, _i64, ctypes.c_int, _f, _f, _f, _f, _f, _f, _vp, ctypes.c_int,
+            _i64, _i32, _i64, ctypes.c_int, _f, _f, _f, _f, _f, _f, _f, _vp, ctypes.c_int,
             _f32p, _f32p, _f32p, _f32p, _u8p, _f32p]
         lib.ora_loco_step.restype = ctypes.c_int
         self.lib = lib
@@ -146,13 +146,13 @@ class Oracle:
             raise ValueError("ora_warmup_step rejected its arguments (%d)" % rc)
         st.step += 1
 
-    def loco_step(self, st, grads, loco_err, beta=0.9, bits=4):
+    def loco_step(self, st, grads, loco_err, beta=0.9, bits=4, ratio=1.0):
         n, W, C = st.n, st.W, st.C
         g = np.ascontiguousarray(grads)
         assert g.size == W * n and loco_err.shape == (W, n)
         codes = np.empty((W, n * bits // 8), np.uint8)
         scales = np.empty((W, n // C), np.float32)
-        rc = self.lib.ora_loco_step(n, W, C, bits, st.b1, st.b2, st.eps, st.lr, st.wd, beta,
+        rc = self.lib.ora_loco_step(n, W, C, bits, st.b1, st.b2, st.eps, st.lr, st.wd, beta, ratio,
                                     g.ctypes.data, grad_code(g), _p(st.x, _f32p),
                                     _p(st.m, _f32p), _p(st.v, _f32p), _p(loco_err, _f32p),
                                     _p(codes, _u8p), _p(scales, _f32p))

@@ -35,7 +35,9 @@
  *  - weight decay is added to the update before the learning rate
  *    (u <- u + wd*x; x <- x - lr*u); bias correction (warm-up only) divides m and v by
  *    (1 - b^t) with the factors given by the caller;
- *  - LoCo: c = g + e~, s = absmax(c over chunk)/L, q = clamp(rint(c/s), -L, L) with
+ *  - LoCo: c = g + ratio*e~ (ratio: the share of the averaged error compensated into
+ *    the gradient, a knob tuned per model and data ["LoCo", key design 2]; 1 by
+ *    default), s = absmax(c over chunk)/L, q = clamp(rint(c/s), -L, L) with
  *    L = 2^(bits-1) - 1 (q = 0 when s = 0), e = c - q*s, e~ <- beta*e~ + (1-beta)*e,
  *    then an (unfrozen) Adam step on the mean of the dequantized gradients.
  *
@@ -292,14 +294,16 @@ int ora_warmup_step(int64_t n, int32_t W, float b1, float b2, float eps, float l
 /* ---- LoCo low-bit step [LoCo "Method"] ------------------------------------------ *
  *
  * loco_err [W][n] holds each worker's moving average of past compensation errors.
- * Per worker: compensate, quantize per chunk to `bits`-bit signed codes with an absmax
+ * Per worker: compensate the gradient with `ratio` times that average (LoCo page, key
+ * design item 2: the proportion of compensation is tuned), quantize per chunk to
+ * `bits`-bit signed codes with an absmax
  * scale, update the moving average with this step's compression error. Then the mean
  * of the W dequantized gradients drives a plain Adam step (m, v and x updated).
  * codes: [W][n*bits/8] bytes (bits = 4: two codes per byte, even element in the low
  * nibble; bits = 8: one signed byte per element); scales [W][n/C].
  */
 int ora_loco_step(int64_t n, int32_t W, int64_t C, int bits,
-                  float b1, float b2, float eps, float lr, float wd, float beta,
+                  float b1, float b2, float eps, float lr, float wd, float beta, float ratio,
                   const void *grads, int dtype,
                   float *x, float *m, float *v, float *loco_err,
                   uint8_t *codes, float *scales)
@@ -322,7 +326,10 @@ int ora_loco_step(int64_t n, int32_t W, int64_t C, int bits,
     for (int32_t w = 0; w < W; ++w) {
         float *et = loco_err + (int64_t)w * n;
         int8_t *qw = q + (int64_t)w * n;
-        for (int64_t i = 0; i < n; ++i) c[i] = ora_grad(grads, dtype, (int64_t)w * n + i) + et[i];
+        for (int64_t i = 0; i < n; ++i) {
+            float comp = ratio * et[i];
+            c[i] = ora_grad(grads, dtype, (int64_t)w * n + i) + comp;
+        }
         for (int64_t k = 0; k < nchunks; ++k) {
             float amax = 0.0f;
             for (int64_t i = k * C; i < (k + 1) * C; ++i) {

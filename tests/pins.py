@@ -27,7 +27,10 @@ What pins what:
   comm_bytes        the pages' 32x (97%) and "up to 5x" communication figures
   loco_*            LoCo codes for exactly representable inputs, nibble layout, the
                     half-step error bound, the moving average's closed form, the
-                    dequantized mean driving a first Adam step (closed form)
+                    dequantized mean driving a first Adam step (closed form); the
+                    compensation ratio: a case worked by hand in dyadic arithmetic at
+                    ratio 1/2 (ties to even included), and ratio 0 making the codes,
+                    scales and (beta = 0) new errors independent of the old errors
 """
 import json
 import math
@@ -453,6 +456,45 @@ def pin_loco_mean(ora):
     want = -1e-4 * c1 * gbar / (np.sqrt(c2) * np.abs(gbar) + 1e-8)
     np.testing.assert_allclose(st.x, want, rtol=2e-6, atol=1e-30)
     np.testing.assert_allclose(st.m, c1 * gbar, rtol=1e-6, atol=0)
+
+
+def pin_loco_ratio_half_by_hand(ora):
+    """One worker, one chunk of four, 4-bit codes, beta = 1/2, ratio = 1/2, every value a
+    small dyadic rational, worked out by hand:
+      c   = g + e~/2         = [7/8, 0, 5/16, -3/16]
+      s   = (7/8) / 7        = 1/8
+      c/s                    = [7, 0, 5/2, -3/2] -> q = [7, 0, 2, -2] (ties to even)
+      e   = c - q*s          = [0, 0, 1/16, 1/16]
+      e~' = e~/2 + e/2       = [3/8, 1/4, 3/32, -1/32]."""
+    n, W, C = 4, 1, 4
+    g = _f32([[0.5, -0.25, 0.25, -0.125]])
+    err = _f32([[0.75, 0.5, 0.125, -0.125]])
+    st = O.OracleState(n, W, C, x=np.zeros(n), m=np.zeros(n), v=np.zeros(n), lr=1e-4)
+    out = ora.loco_step(st, g, err, beta=0.5, bits=4, ratio=0.5)
+    assert np.array_equal(out["scales"], _f32([[0.125]]))
+    assert out["codes"].tolist() == [[0x07, (2 & 0xF) | ((-2 & 0xF) << 4)]]
+    assert np.array_equal(err, _f32([[0.375, 0.25, 0.09375, -0.03125]]))
+
+
+def pin_loco_ratio_zero(ora):
+    """With ratio 0 the gradient is quantized as it is: codes and scales do not depend on
+    the averaged errors, the scale is the chunk's max |g| / 7, and with beta = 0 the new
+    average is the new error alone, the same whatever the old one was."""
+    rng = np.random.default_rng(77)
+    n, W, C = 2048, 2, 256
+    g = (rng.standard_normal((W, n)) * 1e-3).astype(np.float32)
+    outs, errs = [], []
+    for scale in (0.0, 1e-3, -5e-3):
+        st = _rand_state(rng, n, W, C)
+        err = (rng.standard_normal((W, n)) * scale).astype(np.float32)
+        outs.append(ora.loco_step(st, g, err, beta=0.0, bits=4, ratio=0.0))
+        errs.append(err)
+    for o, e in zip(outs[1:], errs[1:]):
+        assert np.array_equal(o["codes"], outs[0]["codes"])
+        assert np.array_equal(o["scales"], outs[0]["scales"])
+        assert np.array_equal(e, errs[0])
+    amax = np.abs(g).reshape(W, -1, C).max(2)
+    np.testing.assert_allclose(outs[0]["scales"], amax / 7, rtol=1e-7)
 
 
 PINS = {name[4:]: fn for name, fn in sorted(globals().items())

@@ -45,8 +45,10 @@ MUTANTS = [
     ("loco_no_average", "float new_part = keep * e;", "float new_part = e;", 0),
     ("loco_scale_levels", "float s = amax / flevels;", "float s = amax / (flevels + 1.0f);", 0),
     ("loco_drop_compensation",
-     "c[i] = ora_grad(grads, dtype, (int64_t)w * n + i) + et[i];",
+     "c[i] = ora_grad(grads, dtype, (int64_t)w * n + i) + comp;",
      "c[i] = ora_grad(grads, dtype, (int64_t)w * n + i);", 0),
+    ("loco_ratio_ignored", "float comp = ratio * et[i];", "float comp = et[i];", 0),
+    ("loco_ratio_on_average", "float old_part = beta * et[i];", "float old_part = beta * ratio * et[i];", 0),
 ]
 
 
