@@ -37,6 +37,7 @@ struct ob_ctx {
     int64_t n = 0, C = 0, nchunks = 0;
     int W = 0;
     float b1 = 0, b2 = 0, eps = 0, lr = 0, wd = 0;
+    float loco_ratio = 1.0f;    // LoCo: share of the averaged error compensated into g
     int bias_correction = 0;
     int64_t step = 0;
     int device = -1;
@@ -322,6 +323,13 @@ int ob_set_options(ob_ctx* c, float weight_decay, int bias_correction)
     return OB_OK;
 }
 
+int ob_set_loco_ratio(ob_ctx* c, float ratio)
+{
+    if (!c || !finite(ratio) || ratio < 0.0f || ratio > 1.0f) return OB_EINVAL;
+    c->loco_ratio = ratio;
+    return OB_OK;
+}
+
 int ob_set_step(ob_ctx* c, int64_t step)
 {
     if (!c || step < 0) return OB_EINVAL;
@@ -570,6 +578,7 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     a.cg_div = make_fastdiv((uint32_t)(c->C / 256));
     a.W = c->W;
     a.bits = bits;
+    a.ratio = c->loco_ratio;
     a.beta = beta;
     a.keep = 1.0f - beta;
     a.b1 = c->b1;

@@ -206,6 +206,76 @@ __device__ __forceinline__ void sum2_add_sq(Sum2& a, float z)
     a.e = __fadd_rn(a.e, __fadd_rn(q, r));
 }
 
+// (a.s + a.e) + (b.s + b.e) as a float pair: the sum of the leading parts split exactly
+// by two-sum, the trailing parts added to its error. Symmetric in a and b bit for bit.
+__device__ __forceinline__ Sum2 sum2_add(const Sum2& a, const Sum2& b)
+{
+    const float t = __fadd_rn(a.s, b.s);
+    const float bp = __fsub_rn(t, a.s);
+    const float ap = __fsub_rn(t, bp);
+    const float q = __fadd_rn(__fsub_rn(a.s, ap), __fsub_rn(b.s, bp));
+    return Sum2{t, __fadd_rn(__fadd_rn(a.e, b.e), q)};
+}
+
+__device__ __forceinline__ Sum2 shfl_xor(const Sum2& v, int o)
+{
+    return Sum2{__shfl_xor_sync(kFull, v.s, o), __shfl_xor_sync(kFull, v.e, o)};
+}
+
+// Warp totals of R rows of float-pair sums, by reduce-scatter: at each of the first
+// log2(P2) exchange distances (16, 8, ...) a lane hands its partner half of its remaining
+// rows and keeps the other half, so the rows spread over the lanes; a butterfly over the
+// remaining distances then leaves every lane with the total of one row, `row` (rows R and
+// above of the power-of-two padding are zeros). 2(P2 - 1 + 5 - log2 P2) shuffles instead
+// of the 10 R of R separate butterflies; the order of the additions is fixed.
+template <int R>
+__device__ __forceinline__ Sum2 warp_reduce_rows(const Sum2 (&v)[R], int lane, int& row)
+{
+    constexpr int P2 = R <= 1 ? 1 : (R <= 2 ? 2 : (R <= 4 ? 4 : (R <= 8 ? 8 : 16)));
+    Sum2 x[P2];
+#pragma unroll
+    for (int i = 0; i < P2; ++i) x[i] = i < R ? v[i] : Sum2{0.0f, 0.0f};
+    int base = 0;
+    int o = 16;
+#pragma unroll
+    for (int half = P2 / 2; half >= 1; half >>= 1, o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const Sum2 recv = shfl_xor(upper ? x[i] : x[i + half], o);
+            x[i] = sum2_add(upper ? x[i + half] : x[i], recv);
+        }
+        if (upper) base += half;
+    }
+#pragma unroll
+    for (; o >= 1; o >>= 1) x[0] = sum2_add(x[0], shfl_xor(x[0], o));
+    row = base;
+    return x[0];
+}
+
+// sqrt(sum / C) rounded to float32, from a sum of squares held as a float pair, in
+// double-float arithmetic (T. J. Dekker, "A floating-point technique for extending the
+// available precision", 1971): the quotient's exact remainder by FMA gives its trailing
+// part, and one Newton correction from the square root's exact residual gives the root
+// to about 2^-46 relative before the single final rounding -- the float32 nearest the
+// exact root except within that distance of a rounding tie. C must be exactly
+// representable (C <= 2^24). Returns false for a mean square outside [2^-80, 2^127] or a
+// non-finite sum (degenerate chunks: the caller recomputes them in double).
+__device__ __forceinline__ bool rms_from_pair(const Sum2& t, float Cf, float& out)
+{
+    const float hi = __fadd_rn(t.s, t.e);
+    const float lo = __fsub_rn(t.e, __fsub_rn(hi, t.s));        // |t.s| >= |t.e|: exact
+    if (!(hi >= __fmul_rn(Cf, 0x1p-80f) && hi <= 0x1p127f)) return false;
+    const float qh = __fdiv_rn(hi, Cf);
+    const float r = __fmaf_rn(-qh, Cf, hi);                      // hi - qh*C, exact
+    const float ql = __fdiv_rn(__fadd_rn(r, lo), Cf);
+    const float sh = __fsqrt_rn(qh);
+    const float d = __fadd_rn(__fmaf_rn(-sh, sh, qh), ql);      // qh - sh^2 exact, then + ql
+    const float sl = __fdiv_rn(d, __fadd_rn(sh, sh));
+    out = __fadd_rn(sh, sl);
+    return true;
+}
+
 // Butterfly sum: every lane ends with the same, order-fixed value.
 __device__ __forceinline__ double warp_sum(double v)
 {
@@ -334,40 +404,48 @@ __device__ __forceinline__ void combine_chunk(const Part& pt, int wpr, int64_t k
     if (lane == 0) cnt[k] = 0u;
 }
 
-// Scales of a chunk whose only contributor is this warp (a chunk that lies wholly inside
-// the range of a warp working alone): its partial is the chunk's total -- the combination
-// would only add zeros to it -- so the scales are written at once, with no fence and no
-// counter. Lane 0 has stored the partials (row r's at idx0 + r*P*J); lane r reads row r's
-// back and forms its scale, all rows at once.
+// Scales of a chunk whose only contributor is this warp, straight from the lanes' float
+// pairs: no partial is stored and no double arithmetic runs (double throughput is low on
+// this part, and with short chunks this runs once per group). The rows' totals are first
+// spread over the lanes (warp_reduce_rows, inline: the sums are in registers); then each
+// row's holder forms and stores its scale. Rows whose sum is degenerate (or chunks too
+// long for a float32 C, which never lie inside one warp's range in practice) are
+// recomputed in double from the stored buffer.
 template <int R>
-__device__ __forceinline__ void sole_chunk(const Part& pt, int64_t k, const double* part, int64_t idx0,
-                                           float* scale_out, int64_t C, const float* rows,
-                                           int64_t row_stride, int lane)
+__device__ __forceinline__ void sole_scales(Sum2 t, int row, const Part& pt, int64_t k, float* scale_out,
+                                            int64_t C, const float* rows, int64_t row_stride, int lane)
 {
-    __syncwarp();                   // orders lane 0's stores before the other lanes' loads
-    double mine = lane < R ? __ldcg(part + idx0 + (int64_t)lane * pt.P * pt.J) : 0.0;
-    unsigned bad = __ballot_sync(kFull, lane < R && !sumsq_trusted(mine, C));
+    constexpr int P2 = R <= 1 ? 1 : (R <= 2 ? 2 : (R <= 4 ? 4 : (R <= 8 ? 8 : 16)));
+    const bool holder = (lane & (32 / P2 - 1)) == 0 && row < R;   // one lane per row
+    float sc = 0.0f;
+    const bool ok = C <= (1 << 24) && rms_from_pair(t, (float)C, sc);
+    unsigned bad = __ballot_sync(kFull, holder && !ok);
+    if (holder && ok) scale_out[(int64_t)row * pt.nchunks + k] = sc;
     if (bad) __threadfence();       // the chunk's rows were just stored by this warp's lanes
     while (bad) {
-        const int r = __ffs(bad) - 1;
+        const int l = __ffs(bad) - 1;
         bad &= bad - 1;
+        const int r = __shfl_sync(kFull, row, l);
         const double ex = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
-        if (lane == r) mine = ex;
+        if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(ex / (double)C);
     }
-    if (lane < R) scale_out[(int64_t)lane * pt.nchunks + k] = (float)sqrt(mine / (double)C);
 }
 
-// After the partials are stored: the only contributor writes the scales; any other counts
-// itself in, and the last one combines.
 template <int R>
-__device__ __forceinline__ void flush_rest(const Part& pt, int wpr, int64_t k, bool sole, int64_t idx0,
-                                           double* part, unsigned* cnt, float* scale_out, int64_t C,
-                                           const float* rows, int64_t row_stride, int lane)
+__device__ __noinline__ void sole_scales_outlined(float ts, float te, int row, const Part& pt, int64_t k,
+                                                  float* scale_out, int64_t C, const float* rows,
+                                                  int64_t row_stride, int lane)
 {
-    if (sole) {
-        sole_chunk<R>(pt, k, part, idx0, scale_out, C, rows, row_stride, lane);
-        return;
-    }
+    sole_scales<R>(Sum2{ts, te}, row, pt, k, scale_out, C, rows, row_stride, lane);
+}
+
+// After the partials are stored: every contributor counts itself in, and the last one
+// combines.
+template <int R>
+__device__ __forceinline__ void flush_rest(const Part& pt, int wpr, int64_t k, double* part, unsigned* cnt,
+                                           float* scale_out, int64_t C, const float* rows, int64_t row_stride,
+                                           int lane)
+{
     __threadfence();
     unsigned last = 0;
     if (lane == 0) {
@@ -383,11 +461,11 @@ __device__ __forceinline__ void flush_rest(const Part& pt, int wpr, int64_t k, b
 // Out-of-line forms, so that a register-hungry kernel does not carry this code's
 // registers through its streaming loop (it runs once per chunk and range).
 template <int R>
-__device__ __noinline__ void flush_rest_outlined(const Part& pt, int wpr, int64_t k, bool sole, int64_t idx0,
-                                                 double* part, unsigned* cnt, float* scale_out, int64_t C,
-                                                 const float* rows, int64_t row_stride, int lane)
+__device__ __noinline__ void flush_rest_outlined(const Part& pt, int wpr, int64_t k, double* part, unsigned* cnt,
+                                                 float* scale_out, int64_t C, const float* rows,
+                                                 int64_t row_stride, int lane)
 {
-    flush_rest<R>(pt, wpr, k, sole, idx0, part, cnt, scale_out, C, rows, row_stride, lane);
+    flush_rest<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
 }
 
 template <int R>
@@ -402,21 +480,37 @@ __device__ __noinline__ void combine_chunk_outlined(const Part& pt, int wpr, int
 // kernel's register pressure (measured per kernel).
 enum FlushCode {
     kFlushInline,       // everything inline
-    kFlushTailCall,     // one call for everything after the partial stores
-    kFlushLastCall      // no shortcut for an only contributor; counter inline; a call only
-                        // for the last contributor's combination
+    kFlushTailCall,     // one call for everything after the partial stores (and one for
+                        // an only contributor's scales)
+    kFlushLastCall      // counter inline; a call only for the last contributor's combination
 };
 
-// Flush this warp's sums of squares of chunk k (rows 0..R-1) as one double partial per row,
-// then finish the chunk if this warp is its only or its last contributor. The warp works
-// range q (groups g0..g1, first chunk kfirst) as warp wir of wpr.
-template <int R, FlushCode CODE>
+// Flush this warp's sums of squares of chunk k (rows 0..R-1): if the chunk lies wholly
+// inside the warp's range, form its scales at once (sole_scales); otherwise store one
+// double partial per row and finish the chunk if this warp is its last contributor. The
+// warp works range q (groups g0..g1, first chunk kfirst) as warp wir of wpr. A caller
+// whose ranges are shared by several warps passes MAYBE_SOLE = false, which leaves the
+// first branch out of its code.
+template <int R, FlushCode CODE, bool MAYBE_SOLE = true>
 __device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, int wir, int64_t k,
                                             int64_t kfirst, int64_t g0, int64_t g1, Sum2 (&acc)[R],
                                             double* part, unsigned* cnt, float* scale_out, int64_t C,
                                             const float* rows, int64_t row_stride, int lane)
 {
     const int64_t idx0 = (q * wpr + wir) * pt.J + (k - kfirst);     // row 0's slot
+    if (MAYBE_SOLE && wpr == 1 && k * pt.CG >= g0 && (k + 1) * pt.CG <= g1) {
+        // the chunk lies wholly inside this warp's range: it is the only contributor
+        int row;
+        const Sum2 t = warp_reduce_rows<R>(acc, lane, row);
+        if (CODE == kFlushTailCall) sole_scales_outlined<R>(t.s, t.e, row, pt, k, scale_out, C, rows, row_stride, lane);
+        else sole_scales<R>(t, row, pt, k, scale_out, C, rows, row_stride, lane);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            acc[r].s = 0.0f;
+            acc[r].e = 0.0f;
+        }
+        return;
+    }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
@@ -424,11 +518,10 @@ __device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, 
         acc[r].s = 0.0f;
         acc[r].e = 0.0f;
     }
-    const bool sole = wpr == 1 && k * pt.CG >= g0 && (k + 1) * pt.CG <= g1;
     if (CODE == kFlushInline) {
-        flush_rest<R>(pt, wpr, k, sole, idx0, part, cnt, scale_out, C, rows, row_stride, lane);
+        flush_rest<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
     } else if (CODE == kFlushTailCall) {
-        flush_rest_outlined<R>(pt, wpr, k, sole, idx0, part, cnt, scale_out, C, rows, row_stride, lane);
+        flush_rest_outlined<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
     } else {
         __threadfence();
         unsigned last = 0;

@@ -6,7 +6,9 @@
 
 namespace ob {
 
-// Division by a run-time constant for 32-bit operands, by a precomputed multiplier:
+// Division by a run-time constant for 32-bit operands, by a precomputed multiplier -- the
+// unsigned division by an invariant integer of T. Granlund and P. L. Montgomery, "Division
+// by Invariant Integers using Multiplication" (PLDI 1994):
 // n / d == (t + ((n - t) >> 1)) >> (l - 1) with t = high 32 bits of n * m,
 // l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1 (d >= 2; d == 1 is passed through).
 struct FastDiv {
@@ -129,7 +131,7 @@ struct LocoArgs {
     int64_t n, C, nchunks, NG;
     FastDiv ng_div, cg_div;    // division by the groups per row / per chunk
     int W, bits;
-    float beta, keep, b1, c1, b2, c2, eps, lr, wd;
+    float ratio, beta, keep, b1, c1, b2, c2, eps, lr, wd;
 };
 
 // Launchers (return the launch status). `grid` blocks of kBlock threads.

@@ -5,12 +5,13 @@
 //
 // Method: "LoCo: Low-Bit Communication Adaptor for Large-scale Model Training",
 // "Method" (moving average of historical compensation errors, compensate before
-// compression, then synchronise) and the abstract (compatible with Adam).
+// compression, then synchronise), key design item 2 (the proportion of the compensation
+// is tuned: `ratio`, 1 by default) and the abstract (compatible with Adam).
 //
 // Three passes. The absmax of c = g + e~ over a chunk must be known before any element
 // of the chunk can be quantized, and a chunk spans up to n/W elements, so c is formed
 // twice (pass 1 for the absmax, pass 2 to quantize) instead of being stored.
-//   pass 1  amax[w][k] = max |g + e~|                (atomicMax on float bits: exact)
+//   pass 1  amax[w][k] = max |c|, c = g + ratio*e~     (atomicMax on float bits: exact)
 //   pass 2  s = amax/L; q = clamp(rint(c/s), -L, L) (0 when s = 0); e = c - q*s;
 //           e~ = beta*e~ + (1-beta)*e; codes <- q
 //   pass 3  gbar = (sum over w of q_w*s_w)/W; Adam on m, v, x
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kBlock) k_loco_absmax(LocoArgs a)
                 float gv[8];
                 gr[u].widen(gv);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) run = fmaxf(run, fabsf(__fadd_rn(gv[j], ev[u][j])));
+                for (int j = 0; j < 8; ++j) run = fmaxf(run, fabsf(__fadd_rn(gv[j], __fmul_rn(a.ratio, ev[u][j]))));
             }
         }
     }
@@ -92,14 +93,14 @@ __global__ void __launch_bounds__(kBlock) k_loco_absmax(LocoArgs a)
 // moving average of the errors in place; returns the codes packed as stored.
 template <int BITS>
 __device__ __forceinline__ void quantize8(const float (&gv)[8], float (&ev)[8], float s, float inv,
-                                          float beta, float keep, uint32_t& lo, uint32_t& hi)
+                                          float ratio, float beta, float keep, uint32_t& lo, uint32_t& hi)
 {
     const float L = (float)((1 << (BITS - 1)) - 1);
     constexpr float kTieMargin = (float)(1 << (BITS - 1)) * 0x1p-21f;   // (L + 1) 2^-21
     int qv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float c = __fadd_rn(gv[j], ev[j]);
+        const float c = __fadd_rn(gv[j], __fmul_rn(ratio, ev[j]));
         int qi = 0;
         if (s > 0.0f) {
             // rint(c/s) with c/s correctly rounded, as defined. |c/s| <= L(1+u), and
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
                 float gv[8];
                 gr[u].widen(gv);
                 uint32_t lo, hi;
-                quantize8<BITS>(gv, ev[u], s, inv, a.beta, a.keep, lo, hi);
+                quantize8<BITS>(gv, ev[u], s, inv, a.ratio, a.beta, a.keep, lo, hi);
                 const int64_t e0 = t * 256 + lane * 8;
                 st8_stream(a.err + e0, ev[u]);
                 uint8_t* out = a.codes + e0 * BITS / 8;

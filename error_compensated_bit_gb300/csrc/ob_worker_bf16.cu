@@ -1,0 +1,42 @@
+// Worker kernels for __nv_bfloat16 gradients (all W, both range modes); see ob_worker.cuh.
+#include "ob_worker.cuh"
+
+namespace ob {
+
+cudaError_t launch_worker_bf16(int W, const WorkerArgs& a, int grid, cudaStream_t s, int smem_budget)
+{
+    switch (W) {
+#define OB_CASE(w) \
+    case w:        \
+        return launch_wg<w, __nv_bfloat16>(a, grid, s, smem_budget);
+        OB_FOR_EACH_W(OB_CASE)
+#undef OB_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_worker_bf16(int W, int smem_budget)
+{
+    switch (W) {
+#define OB_CASE(w) \
+    case w:        \
+        return prepare_wg<w, __nv_bfloat16>(smem_budget);
+        OB_FOR_EACH_W(OB_CASE)
+#undef OB_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+WorkerConfig worker_config_bf16(int W, int smem_budget)
+{
+    switch (W) {
+#define OB_CASE(w) \
+    case w:        \
+        return config_w<w, __nv_bfloat16>(smem_budget);
+        OB_FOR_EACH_W(OB_CASE)
+#undef OB_CASE
+    }
+    return WorkerConfig{};
+}
+
+}  // namespace ob

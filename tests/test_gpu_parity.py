@@ -106,12 +106,16 @@ def test_weight_decay_parity(ora):
     _free_run(ora, st, lambda t: _grads(rng, W, n, "f16"), 3)
 
 
+@pytest.mark.parametrize("C", [256 * 16, 256])
 @pytest.mark.parametrize("case", ["zeros", "negzero", "single", "negative", "subnormal",
-                                  "mask_all_zero", "huge_range"])
-def test_edge_cases(ora, case):
+                                  "mask_all_zero", "huge_range", "overflow"])
+def test_edge_cases(ora, case, C):
+    """C = 4096 spreads every chunk over several warp ranges (partials combined by the
+    last contributor); C = 256 puts every chunk inside one warp's range (scales formed by
+    that warp alone). Degenerate chunks -- all zero, subnormal, or sums of squares that
+    overflow float32 -- take the double-precision fallback in both."""
     rng = np.random.default_rng(5)
     W, n = 4, 4 * 256 * 64
-    C = 256 * 16
     mask = None
     st = random_state(rng, n, W, C)
     g = np.zeros((W, n), np.float32)
@@ -131,6 +135,10 @@ def test_edge_cases(ora, case):
         st.mask = np.zeros(n, np.uint8)
     elif case == "huge_range":
         g = _grads(rng, W, n, "f32") * np.float32(10.0) ** rng.integers(-12, 6, (W, n)).astype(np.float32)
+    elif case == "overflow":
+        # |z| about 4e18: the squares fit float32 but a chunk's sum of them does not
+        g = (rng.choice([-4e19, 4e19], (W, n)) * rng.uniform(0.5, 1.0, (W, n))).astype(np.float32)
+        g[:, : n // 2] = _grads(rng, W, n // 2, "f32")
     gpu = CudaPath(st, mask=mask)
     tr = Tracker(n, W, C)
     for t in range(3):
@@ -221,18 +229,23 @@ def test_warmup_then_compressed(ora):
             tr.compare(t, gpu.snapshot(), out, st, check_mask=mask)
 
 
-@pytest.mark.parametrize("W,dtype,bits,per_row", [(4, "bf16", 4, 2), (2, "f32", 8, 2), (3, "f16", 4, 2),
-                                                   (4, "bf16", 4, 400), (2, "f32", 8, 25)])
-def test_loco_parity(ora, W, dtype, bits, per_row):
+@pytest.mark.parametrize("W,dtype,bits,per_row,ratio", [
+    (4, "bf16", 4, 2, 1.0), (2, "f32", 8, 2, 1.0), (3, "f16", 4, 2, 1.0),
+    (4, "bf16", 4, 400, 1.0), (2, "f32", 8, 25, 1.0),
+    (4, "bf16", 4, 2, 0.5), (3, "f16", 8, 25, 0.0), (2, "f32", 4, 400, 0.3)])
+def test_loco_parity(ora, W, dtype, bits, per_row, ratio):
     """per_row chunks per worker row: 400 makes every 256-element group a chunk of its
-    own, so a warp's range crosses many scale slots."""
+    own, so a warp's range crosses many scale slots. ratio: the share of the averaged
+    error compensated into the gradient (1 is plain c = g + e~)."""
     from error_compensated_bit_gb300 import ob
-    rng = np.random.default_rng(40 + W + per_row)
+    rng = np.random.default_rng(40 + W + per_row + int(ratio * 10))
     n = W * 256 * 400
     C = n // W // per_row
     st = random_state(rng, n, W, C)
     st.v[:] = 0.0
     gpu = CudaPath(st)
+    if ratio != 1.0:
+        gpu.ctx.set_loco_ratio(ratio)
     err_d = torch.zeros(W, n, dtype=torch.float32, device="cuda")
     lws = torch.zeros(gpu.ctx.loco_workspace_bytes(bits), dtype=torch.uint8, device="cuda")
     err = np.zeros((W, n), np.float32)
@@ -240,7 +253,7 @@ def test_loco_parity(ora, W, dtype, bits, per_row):
     scale_off = (code_bytes + 255) // 256 * 256
     for t in range(4):
         g = _grads(rng, W, n, dtype)
-        out = ora.loco_step(st, g, err, beta=0.9, bits=bits)
+        out = ora.loco_step(st, g, err, beta=0.9, bits=bits, ratio=ratio)
         from gpu_util import to_device_grads
         gpu.ctx.loco_step(to_device_grads(g, "cuda"), gpu.x, gpu.m, gpu.v, err_d, lws, 0.9, bits)
         torch.cuda.synchronize()
