@@ -54,6 +54,7 @@ SIGNATURES = {
     "ob_selftest_wait": (_int, [_vp, _vp, ctypes.c_uint64, _vp]),
     "ob_strerror": (ctypes.c_char_p, [_int]),
     "ob_last_cuda_error": (_int, []),
+    "ob_set_loco_ratio": (_int, [_vp, _f]),
     "ob_worker_compress_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ob_noalloc_read_status": (_int, [_vp, ctypes.POINTER(ctypes.c_uint), _vp]),
 }
@@ -154,6 +155,9 @@ class Context:
 
     def set_options(self, weight_decay=0.0, bias_correction=False):
         _call("ob_set_options", self.h, weight_decay, int(bool(bias_correction)))
+
+    def set_loco_ratio(self, ratio):
+        _call("ob_set_loco_ratio", self.h, float(ratio))
 
     def set_step(self, step):
         _call("ob_set_step", self.h, step)

@@ -190,7 +190,7 @@ int ob_compressed_step_host(ob_ctx *ctx, const void *grads_host, void *grads_dev
 
 /*
  * LoCo step, "LoCo" page, "Method". Per worker w and element i of chunk k:
- *   c = g_w + e~_w;  s_wk = max|c| over chunk / L;  q = clamp(rint(c/s_wk), -L, L)
+ *   c = g_w + ratio*e~_w;  s_wk = max|c| over chunk / L;  q = clamp(rint(c/s_wk), -L, L)
  *   (q = 0 when s_wk = 0), L = 2^(bits-1) - 1;  e~_w = beta*e~_w + (1-beta)*(c - q*s_wk)
  * then gbar = (sum over w of q*s_wk)/W drives a plain Adam step on x, m, v (not
  * frozen). bits is 4 (two codes per byte, even element in the low nibble, two's
@@ -199,6 +199,14 @@ int ob_compressed_step_host(ob_ctx *ctx, const void *grads_host, void *grads_dev
  */
 int ob_loco_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m, float *v,
                  float *loco_err, float beta, int bits, void *loco_ws, void *stream);
+
+/*
+ * The LoCo compensation ratio ("LoCo" page, key design item 2: the proportion of the
+ * compensation applied to the gradient is tuned per model and data): c = g + ratio*e~ in
+ * ob_loco_step, ratio in [0, 1], 1 when never set (ratio 1 is the plain c = g + e~).
+ * OB_EINVAL outside that range.
+ */
+int ob_set_loco_ratio(ob_ctx *ctx, float ratio);
 size_t ob_loco_workspace_bytes(const ob_ctx *ctx, int bits);
 
 /* ---- state ----------------------------------------------------------------------------- */

@@ -104,6 +104,10 @@ def test_calls_reject_bad_arguments(ob):
                                        good, good, S) == ob.OB_EINVAL
     assert lib.ob_set_options(h, -0.1, 0) == ob.OB_EINVAL
     assert lib.ob_set_options(h, 0.01, 1) == ob.OB_OK
+    for bad in (-0.25, 1.5, float("nan"), float("inf")):
+        assert lib.ob_set_loco_ratio(h, bad) == ob.OB_EINVAL
+    for good_ratio in (0.0, 0.5, 1.0):
+        assert lib.ob_set_loco_ratio(h, good_ratio) == ob.OB_OK
     assert lib.ob_set_step(h, -1) == ob.OB_EINVAL
     assert lib.ob_set_step(h, 41) == ob.OB_OK and lib.ob_get_step(h) == 41
     assert lib.ob_set_lr(h, float("inf")) == ob.OB_EINVAL
