@@ -322,7 +322,9 @@ static __device__ __noinline__ double chunk_sumsq_exact(const float* row, int64_
 // warp (a lane's running sums add their terms in ascending range order; the 32 lanes' sums
 // are then combined by a fixed butterfly), then scale = sqrt(sum / C). Loads of several
 // ranges are issued before they are added; a missing term adds +0.0, which leaves a sum of
-// squares unchanged, so the unrolling does not change the result.
+// squares unchanged, so the unrolling does not change the result. (Wider unrolling
+// shortens this on small buffers, where its L2 round trips are a large part of the worker's
+// time, but the larger out-of-line body made the calling kernels spill.)
 template <int R>
 __device__ __forceinline__ void combine_chunk(const Part& pt, int wpr, int64_t k, const double* part,
                                               unsigned* cnt, float* scale_out, int64_t C,

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace ob {
 
 // Division by a run-time constant for 32-bit operands, by a precomputed multiplier -- the
@@ -158,5 +160,25 @@ int occupancy_server(int W);
 int occupancy_update();
 int occupancy_loco_absmax(int dtype);
 int occupancy_loco_quant(int dtype, int bits);
+
+// Launch `kernel` with the programmatic stream-serialization attribute (see pdl_wait in
+// ob_tma.cuh): it may begin while the previous kernel on the stream finishes.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int block, size_t smem, cudaStream_t s,
+                              Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 }  // namespace ob

@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const Part pt = a.pt;
     const int64_t words_per_row = a.n / 32;
+    pdl_wait();             // the worker pass has finished
+    pdl_allow_next();
 
     for (int64_t q = warp; q < pt.P; q += nwarps) {
         const int64_t g0 = range_begin(pt, q);
@@ -178,6 +180,8 @@ __global__ void __launch_bounds__(kBlock, 4) k_server_staged(ServerArgs a)
     const Part pt = a.pt;
     const int64_t words_per_row = a.n / 32;
     const uint64_t pol = policy_evict_first();
+    pdl_wait();             // the worker pass has finished
+    pdl_allow_next();
 
     // this lane's copies of group gi into stage s: two 16-byte pieces of y, and piece
     // (lane & 1) of worker row (lane >> 1)'s 32 bytes of sign words
@@ -287,6 +291,8 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
     constexpr bool masked = MASKED;
     // one contiguous, balanced range of groups per warp (the grid is one resident wave)
     const int64_t g_end = (warp + 1) * a.NG / nwarps;
+    pdl_wait();             // the server pass has finished
+    pdl_allow_next();
 
     for (int64_t gb = warp * a.NG / nwarps; gb < g_end; gb += U) {
         float vv[U][8], xv[U][8];
@@ -349,6 +355,8 @@ __global__ void __launch_bounds__(kBlock) k_scales(UpdateArgs a)
 {
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    pdl_wait();             // the update pass has finished
+    pdl_allow_next();
     for (int64_t i = tid; i < a.nscales_w; i += nthreads) a.s_prev[i] = a.s_next[i];
     for (int64_t i = tid; i < a.nchunks; i += nthreads) a.t_prev[i] = a.t_next[i];
 }
@@ -386,9 +394,8 @@ __global__ void __launch_bounds__(kBlock) k_export(ExportArgs a)
 template <int W>
 static cudaError_t launch_s(const ServerArgs& a, int grid, cudaStream_t s)
 {
-    if constexpr (W > 8) k_server_staged<W><<<grid, kBlock, ServerStage<W>::kSmem, s>>>(a);
-    else k_server<W><<<grid, kBlock, 0, s>>>(a);
-    return cudaGetLastError();
+    if constexpr (W > 8) return launch_pdl(k_server_staged<W>, grid, kBlock, ServerStage<W>::kSmem, s, a);
+    else return launch_pdl(k_server<W>, grid, kBlock, 0, s, a);
 }
 
 template <int W>
@@ -452,9 +459,8 @@ int occupancy_server(int W)
 
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s)
 {
-    if (a.maskbits) k_update<true><<<grid, kBlock, 0, s>>>(a);
-    else k_update<false><<<grid, kBlock, 0, s>>>(a);
-    return cudaGetLastError();
+    if (a.maskbits) return launch_pdl(k_update<true>, grid, kBlock, 0, s, a);
+    return launch_pdl(k_update<false>, grid, kBlock, 0, s, a);
 }
 
 int occupancy_update()
@@ -467,8 +473,7 @@ int occupancy_update()
 
 cudaError_t launch_scales(const UpdateArgs& a, int grid, cudaStream_t s)
 {
-    k_scales<<<grid, kBlock, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_scales, grid, kBlock, 0, s, a);
 }
 
 cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s)

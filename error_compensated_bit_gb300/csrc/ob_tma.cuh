@@ -127,4 +127,22 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Programmatic dependent launch (sm_90+). A kernel launched with the programmatic
+// stream-serialization attribute may start while the kernel before it on the stream is
+// still running; pdl_wait() blocks until that kernel has completed and its writes are
+// visible (it returns at once when there is no such kernel), so it comes before the
+// kernel's first global-memory access, read or write. pdl_allow_next() lets the kernel
+// after this one be scheduled (its blocks then wait in their own pdl_wait()); since every
+// kernel of the chain waits before touching memory, each one also follows all earlier
+// ones.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_allow_next()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace ob

@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
         mbar_init_fence();
     }
     __syncwarp();
+    pdl_wait();             // the previous step's kernels have finished with the buffers
+    pdl_allow_next();
     const uint64_t pol = policy_evict_first();
     uint32_t phase = 0;   // bit s: parity of stage s's next completion
 
@@ -255,9 +257,8 @@ cudaError_t launch_wg(const WorkerArgs& a, int grid, cudaStream_t s, int smem_bu
     if ((int)c.smem_bytes > smem_budget) return cudaErrorInvalidConfiguration;
     WorkerArgs b = a;
     b.stages = c.stages;
-    if (a.interleave) k_worker<W, G, true><<<grid, c.warps_per_block * 32, c.smem_bytes, s>>>(b);
-    else k_worker<W, G, false><<<grid, c.warps_per_block * 32, c.smem_bytes, s>>>(b);
-    return cudaGetLastError();
+    if (a.interleave) return launch_pdl(k_worker<W, G, true>, grid, c.warps_per_block * 32, c.smem_bytes, s, b);
+    return launch_pdl(k_worker<W, G, false>, grid, c.warps_per_block * 32, c.smem_bytes, s, b);
 }
 
 // The shared-memory opt-in of the worker kernels for W, on the current device. It is a
