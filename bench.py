@@ -88,6 +88,11 @@ def worker_bytes_per_elem(W, s_g):
 L2_BYTES = 129 * 1000 * 1000        # GB300 L2 (129 MB)
 
 
+# the worker kernel's sources (its DRAM traffic record is valid only while they match)
+WORKER_SOURCES = ["ob_worker.cuh", "ob_worker_f32.cu", "ob_worker_f16.cu", "ob_worker_bf16.cu",
+                  "ob_common.cuh", "ob_tma.cuh", "ob_internal.h"]
+
+
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -356,50 +361,65 @@ class Run:
         # L2 is flushed (a 2x-L2 buffer written) before every step, outside per-step events
         flush = b_step < 8 * L2_BYTES
         scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps if flush else 1)]
-        launches0 = ctx.launch_count()
-        ctx.profile(True)
-        if barrier_fn:
-            barrier_fn()
-        torch.cuda.synchronize(dev)
-        if clocks:
-            clocks.start()
-            time.sleep(0.3)
         s = self.stream
-        if not flush:
-            ev[0][0].record(s)
-        for t in range(steps):
-            if flush:
-                scratch.fill_(float(t))
-                ev[t][0].record(s)
-            if cuda_graph is not None:
-                cuda_graph[t % GRAD_BUFFERS].replay()
-            else:
-                self.step()
-            if flush:
-                ev[t][1].record(s)
-        if not flush:
-            ev[0][1].record(s)
-        torch.cuda.synchronize(dev)
-        clk = clocks.stop() if clocks else None
-        if barrier_fn:
-            barrier_fn()
-        ms_total = sum(a.elapsed_time(b) for a, b in ev)
-        launches = ctx.launch_count() - launches0
+
+        def timed_loop(kernel_events):
+            """`steps` steps; per-step events when flushing, else one pair around all."""
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps if flush else 1)]
+            ctx.profile(kernel_events)
+            launches0 = ctx.launch_count()
+            if barrier_fn:
+                barrier_fn()
+            torch.cuda.synchronize(dev)
+            if clocks:
+                clocks.start()
+                time.sleep(0.3)
+            if not flush:
+                ev[0][0].record(s)
+            for t in range(steps):
+                if flush:
+                    scratch.fill_(float(t))
+                    ev[t][0].record(s)
+                if cuda_graph is not None:
+                    cuda_graph[t % GRAD_BUFFERS].replay()
+                else:
+                    self.step()
+                if flush:
+                    ev[t][1].record(s)
+            if not flush:
+                ev[0][1].record(s)
+            torch.cuda.synchronize(dev)
+            clk = clocks.stop() if clocks else None
+            if barrier_fn:
+                barrier_fn()
+            return sum(a.elapsed_time(b) for a, b in ev), ctx.launch_count() - launches0, clk
+
+        # Per-kernel events (recorded by the library around each launch) time the kernels;
+        # on a step of a few tens of microseconds they also lengthen it (each pair splits
+        # the launch chain), so a flushed small step is timed once without them for the
+        # step time and once with them for the kernel times.
+        separate = flush and cuda_graph is None
+        if separate:
+            ms_total, launches, clk = timed_loop(False)
+            kernels_ms, _, _ = timed_loop(True)
+        else:
+            ms_total, launches, clk = timed_loop(cuda_graph is None)
+            kernels_ms = ms_total
         if cuda_graph is not None:   # replays launch the captured kernels without the library's counter
             launches = steps * graph_launches
         per_kernel = {}
         for k, name in self.ob.KERNEL_NAMES.items():
             t_ms, cnt = ctx.profile_read(k)
             if cnt:
-                per_kernel[name] = {"launches": cnt, "avg_us": 1e3 * t_ms / cnt, "share": t_ms / ms_total}
+                per_kernel[name] = {"launches": cnt, "avg_us": 1e3 * t_ms / cnt, "share": t_ms / kernels_ms}
         ctx.profile(False)
         del scratch
         dom = KERNEL_OF_PHASE[self.phase]
         k_bytes = dominant_kernel_bytes(self.phase, self.wl.n, self.wl.W, self.wl.grad_bytes)
         k_avg_us = per_kernel[dom]["avg_us"] if dom in per_kernel else None
         return {"ms_total": ms_total, "steps": steps, "b_step": b_step, "flush": flush,
+                "kernel_events_pass": "separate" if separate else "same",
                 "kernels": per_kernel, "launches": launches, "clocks": clk,
                 "cuda_graph": cuda_graph is not None, "dominant": dom, "k_bytes": k_bytes,
                 "k_avg_us": k_avg_us}
@@ -430,6 +450,8 @@ def summarize(run, res, peak):
             "bytes_per_step": res["b_step"], "dominant": dom,
             "kernels": {k: {"avg_us": v["avg_us"], "share": v["share"]} for k, v in res["kernels"].items()},
             "cuda_graph": res["cuda_graph"], "l2": "flushed before every step" if res["flush"] else "streamed (step >> L2)",
+            "kernel_times": ("a second timed pass with per-kernel events (shares of that pass)"
+                             if res["kernel_events_pass"] == "separate" else "per-kernel events in the timed pass"),
             "gpu_launches": res["launches"], "clocks": res["clocks"]}
 
 
@@ -541,7 +563,7 @@ def gpu_arm(args, wl):
     k_avg_s = res["k_avg_us"] / 1e6 if res["k_avg_us"] else None
     achieved = res["k_bytes"] / k_avg_s / 1e9 if k_avg_s else None
     if args.phase == "compressed":
-        khash = kernel_source_hash(["ob_worker.cu", "ob_common.cuh", "ob_tma.cuh"])
+        khash = kernel_source_hash(WORKER_SOURCES)
     elif args.phase == "warmup":
         khash = kernel_source_hash(["ob_warmup.cu", "ob_common.cuh"])
     else:
