@@ -53,16 +53,33 @@ __device__ __forceinline__ uint64_t transpose8x8(uint64_t x)
 // a = (sum over w ascending of +-S_wk)/W;  e_s = yprev - T_prev*sign(yprev);  y = a + e_s;
 // bit = (y >= 0); ybuf = y; chunk sums of y^2 -> T_next.
 // Memory per element: W/8 (worker bits) + 4 + 4 (y) + 1/8 (server bits).
+// This lane's sign bytes of group gi from every worker row: byte (lane & 3) of word
+// (lane >> 2) of the group's eight words in row w becomes byte w of the result (rows W
+// and above give zero bytes). Two rounds of byte permutes gather four rows into one word.
+template <int W>
+__device__ __forceinline__ uint64_t gather_sign_bytes(const uint32_t* wbits, int64_t words_per_row, int64_t gi,
+                                                      int lane)
+{
+    const uint32_t* p = wbits + gi * 8 + (lane >> 2);
+    uint32_t wv[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) wv[w] = w < W ? __ldcs(p + (int64_t)w * words_per_row) : 0u;
+    const uint32_t b = (uint32_t)lane & 3u;
+    const uint32_t pick = b | ((b + 4u) << 4);        // byte b of the first and of the second word
+    const uint32_t lo = __byte_perm(__byte_perm(wv[0], wv[1], pick), __byte_perm(wv[2], wv[3], pick), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(wv[4], wv[5], pick), __byte_perm(wv[6], wv[7], pick), 0x5410);
+    return ((uint64_t)hi << 32) | lo;
+}
+
 // Used for W <= 8: one group's loads per warp in flight, 64 registers (four blocks per SM).
 // Keeping several groups in flight through shared memory (k_server_staged) measured slower
 // here, where the pass is close to bound by instruction issue; it pays for W > 8.
 template <int W>
 __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
 {
-    constexpr int T = W < 8 ? W : 8;     // workers covered by the table
-    constexpr int U = W > 8 ? 2 : 1;     // groups per iteration
-    __shared__ float s_tab[(kBlock / 32) << T];
-    float* tab = s_tab + ((threadIdx.x >> 5) << T);
+    static_assert(W <= 8, "the register server pass covers up to eight workers");
+    __shared__ float s_tab[(kBlock / 32) << W];
+    float* tab = s_tab + ((threadIdx.x >> 5) << W);
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -85,9 +102,9 @@ __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
         build_average_table<W>(tab, sw, lane);
         Sum2 acc[1] = {{0.0f, 0.0f}};
 
-        for (int64_t gi = g0; gi < g1;) {
+        for (int64_t gi = g0; gi < g1; ++gi) {
             if (gi == kend) {
-                flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+                flush_chunk<1, kFlushInline>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
                 ++k;
                 kend += pt.CG;
 #pragma unroll
@@ -95,55 +112,25 @@ __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
                 tp = __ldg(a.t_prev + k);
                 build_average_table<W>(tab, sw, lane);
             }
-            // with W > 8 two groups of a chunk are in flight per iteration
-            const int nu = (U == 2 && gi + 1 < g1 && gi + 1 != kend) ? 2 : 1;
-            uint32_t bytes[U][W];
-            float yv[U][8];
+            const uint64_t raw = gather_sign_bytes<W>(a.wbits, words_per_row, gi, lane);
+            float yv[8];
+            ld8_stream(a.ybuf + gi * 256 + lane * 8, yv);
+            const uint64_t pat = transpose8x8(raw);   // byte j: element j's signs, bit w = worker w
+            uint32_t byte = 0;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (u < nu) {
-#pragma unroll
-                    for (int w = 0; w < W; ++w) bytes[u][w] = lane_byte(a.wbits + (int64_t)w * words_per_row, gi + u, lane);
-                    ld8_stream(a.ybuf + (gi + u) * 256 + lane * 8, yv[u]);
-                }
+            for (int j = 0; j < 8; ++j) {
+                const float avg = tab[(uint32_t)(pat >> (8 * j)) & 0xffu];
+                const float es = __fsub_rn(yv[j], signed_scale(tp, yv[j] >= 0.0f));
+                const float y = __fadd_rn(avg, es);
+                yv[j] = y;
+                byte |= (y >= 0.0f ? 1u : 0u) << j;
+                sum2_add_sq(acc[0], y);
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (u < nu) {
-                    const int64_t gu = gi + u;
-                    uint64_t lo = 0, hi = 0;
-#pragma unroll
-                    for (int w = 0; w < T; ++w) lo |= (uint64_t)bytes[u][w] << (8 * w);
-                    lo = transpose8x8(lo);
-                    if (W > 8) {
-#pragma unroll
-                        for (int w = 8; w < W; ++w) hi |= (uint64_t)bytes[u][w] << (8 * (w - 8));
-                        hi = transpose8x8(hi);
-                    }
-                    uint32_t byte = 0;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float avg = tab[(uint32_t)(lo >> (8 * j)) & 0xffu];
-                        if (W > 8) {
-                            const uint32_t pat = (uint32_t)(hi >> (8 * j)) & 0xffu;
-#pragma unroll
-                            for (int w = 8; w < W; ++w) avg = __fadd_rn(avg, signed_scale(sw[w], (pat >> (w - 8)) & 1u));
-                            avg = (W & (W - 1)) == 0 ? __fmul_rn(avg, 1.0f / (float)W) : __fdiv_rn(avg, (float)W);
-                        }
-                        const float es = __fsub_rn(yv[u][j], signed_scale(tp, yv[u][j] >= 0.0f));
-                        const float y = __fadd_rn(avg, es);
-                        yv[u][j] = y;
-                        byte |= (y >= 0.0f ? 1u : 0u) << j;
-                        sum2_add_sq(acc[0], y);
-                    }
-                    st8_stream(a.ybuf + gu * 256 + lane * 8, yv[u]);
-                    const uint32_t word = quad_word(byte, lane);
-                    if ((lane & 3) == 0) __stcs(a.sbits + gu * 8 + (lane >> 2), word);
-                }
-            }
-            gi += nu;
+            st8_stream(a.ybuf + gi * 256 + lane * 8, yv);
+            const uint32_t word = quad_word(byte, lane);
+            if ((lane & 3) == 0) __stcs(a.sbits + gi * 8 + (lane >> 2), word);
         }
-        flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+        flush_chunk<1, kFlushInline>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
 }
 
