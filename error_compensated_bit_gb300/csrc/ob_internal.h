@@ -54,6 +54,8 @@ struct WorkerArgs {
     float b1, c1;
     int stages;             // pipeline stages per warp (set by the launcher)
     int interleave;         // 1: one range per block, warps interleaved; 0: one range per warp
+    int block_combine;      // interleaved: the block's warps pre-combine their partials (launcher)
+    uint32_t bars_off, stages_off, bcnt_off;   // dynamic shared-memory layout (launcher)
 };
 
 // Launch shape of the worker kernel for one (W, gradient type).
@@ -62,6 +64,8 @@ struct WorkerConfig {
     int stages;
     size_t smem_bytes;
     uint32_t stage_bytes;
+    int block_combine;      // room for the block-level partials without fewer warps or stages
+    uint32_t bars_off, stages_off, bcnt_off;
 };
 
 struct ServerArgs {

@@ -47,7 +47,74 @@ struct WorkerStage {
 
 constexpr int kMaxWarps = 16;
 constexpr int kMaxStages = 8;
-constexpr uint32_t kBarBytes = 8 * kMaxWarps * kMaxStages;   // 8-byte mbarriers
+
+// Dynamic shared memory of a worker block: [block partials: double [2][kMaxWarps][W], when
+// the block pre-combines][two counters][mbarriers: warps x stages x 8 B][stages, 128-byte
+// aligned]. The offsets come from config_w through WorkerArgs.
+template <int W>
+constexpr uint32_t block_part_bytes()
+{
+    return 2u * kMaxWarps * W * 8u;
+}
+
+// Whether the interleaved kernel for (W, G) pre-combines its partials in the block (see
+// below): chosen per instantiation, so each kernel carries one flush path. With one block
+// of up to 227 KB per SM it fits beside the stages without costing a warp or a stage
+// except for 16-bit gradients with W >= 11 (16 warps x 7 KB stages fill the block).
+template <int W, typename G>
+constexpr bool block_combine_fits()
+{
+    return !(W >= 11 && sizeof(G) == 2);
+}
+
+// Interleaved mode: the warps of a block share one range, so their partial sums of chunk k
+// are first combined inside the block. Each warp stores its row totals in shared memory
+// and counts itself in; the block's last warp adds them in warp order and flushes one
+// partial per row for the block's range (the slot layout of one warp per range), after
+// which the chunk's last range combines as usual. A chunk then has one partial per range
+// and row instead of one per range, warp and row, so the combination on the step's
+// critical path takes about one round of loads instead of one per few ranges. Slot j = k -
+// (the range's first chunk) is 0 or 1 (interleaved ranges touch at most two chunks), and a
+// block works one range per launch, so no slot is reused within a launch.
+template <int W>
+__device__ __noinline__ void block_flush(const Part& pt, int64_t q, int wpb, int j, int64_t k, const double* bpart,
+                                         double* part, unsigned* cnt, float* scale_out, int64_t C, const float* rows,
+                                         int64_t row_stride, int lane)
+{
+    __syncwarp();
+    __threadfence_block();
+    for (int r = lane; r < W; r += 32) {
+        double sum = 0.0;
+        for (int w = 0; w < wpb; ++w) sum += bpart[(j * kMaxWarps + w) * W + r];
+        part[((int64_t)r * pt.P + q) * pt.J + j] = sum;
+    }
+    __syncwarp();
+    flush_rest<W>(pt, 1, k, part, cnt, scale_out, C, rows, row_stride, lane);
+}
+
+template <int W>
+__device__ __forceinline__ void flush_chunk_block(const Part& pt, int64_t q, int wpb, int wib, int64_t k, int64_t kfirst,
+                                                  Sum2 (&acc)[W], double* bpart, unsigned* bcnt, double* part,
+                                                  unsigned* cnt, float* scale_out, int64_t C, const float* rows,
+                                                  int64_t row_stride, int lane)
+{
+    const int j = (int)(k - kfirst);
+#pragma unroll
+    for (int r = 0; r < W; ++r) {
+        const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
+        if (lane == 0) bpart[(j * kMaxWarps + wib) * W + r] = d;
+        acc[r].s = 0.0f;
+        acc[r].e = 0.0f;
+    }
+    unsigned prev = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        prev = atomicAdd(bcnt + j, 1u);
+        __threadfence_block();
+    }
+    prev = __shfl_sync(kFull, prev, 0);
+    if (prev == (unsigned)(wpb - 1)) block_flush<W>(pt, q, wpb, j, k, bpart, part, cnt, scale_out, C, rows, row_stride, lane);
+}
 
 template <typename G>
 __device__ __forceinline__ void ld8_shared(const unsigned char* row, int lane, float (&v)[8]);
@@ -101,9 +168,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
     const int S = a.stages;
     const Part pt = a.pt;
     const int64_t words_per_row = a.n / 32;
-    const uint32_t bar0 = smem_u32(smem) + 8u * (uint32_t)(wib * S);
-    unsigned char* stage0 = smem + kBarBytes + (size_t)wib * S * St::kBytes;
+    const uint32_t bar0 = smem_u32(smem) + a.bars_off + 8u * (uint32_t)(wib * S);
+    unsigned char* stage0 = smem + a.stages_off + (size_t)wib * S * St::kBytes;
     const uint32_t st0 = smem_u32(stage0);
+    constexpr bool bcomb = INTER && block_combine_fits<W, G>();
+    double* bpart = reinterpret_cast<double*>(smem);
+    unsigned* bcnt = reinterpret_cast<unsigned*>(smem + a.bcnt_off);
+    if (bcomb) {
+        if (threadIdx.x == 0) {
+            bcnt[0] = 0u;
+            bcnt[1] = 0u;
+        }
+        __syncthreads();
+    }
 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(bar0 + 8u * s, 1);
@@ -167,7 +244,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
             if (kg != k) {
                 // this warp's part of chunks k .. kg-1 is done (possibly empty)
                 while (k < kg) {
-                    flush_chunk<W, kFlushTailCall, !INTER>(pt, q, wpr, wir, k, kfirst, g0, g1, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+                    if constexpr (bcomb) flush_chunk_block<W>(pt, q, wpb, wib, k, kfirst, acc, bpart, bcnt, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+                    else flush_chunk<W, kFlushTailCall, !INTER>(pt, q, wpr, wir, k, kfirst, g0, g1, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
                     ++k;
                 }
 #pragma unroll
@@ -223,7 +301,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
             }
         }
         for (;;) {
-            flush_chunk<W, kFlushTailCall, !INTER>(pt, q, wpr, wir, k, kfirst, g0, g1, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+            if constexpr (bcomb) flush_chunk_block<W>(pt, q, wpb, wib, k, kfirst, acc, bpart, bcnt, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
+            else flush_chunk<W, kFlushTailCall, !INTER>(pt, q, wpr, wir, k, kfirst, g0, g1, acc, a.part, a.cnt, a.s_next, a.C, a.zbuf, a.n, lane);
             if (k == klast) break;
             ++k;
         }
@@ -232,21 +311,32 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_worker(WorkerArgs a)
 
 // Launch shape for (W, gradient type): warps per block and stages per warp chosen so that
 // the stages fill the shared memory of one block (one block per SM): at least two stages
-// per warp, up to sixteen warps, and as many stages as then fit (at most eight).
+// per warp, up to sixteen warps, and as many stages as then fit (at most eight), after
+// the block-level partials of the interleaved kernels that pre-combine.
 template <int W, typename G>
 WorkerConfig config_w(int smem_budget)
 {
     using St = WorkerStage<W, G>;
-    WorkerConfig c{};
-    const int usable = smem_budget - (int)kBarBytes;
-    int warps = usable / (2 * (int)St::kBytes);
-    warps = warps > kMaxWarps ? kMaxWarps : (warps < 1 ? 1 : warps);
-    int stages = usable / (warps * (int)St::kBytes);
-    stages = stages > kMaxStages ? kMaxStages : (stages < 2 ? 2 : stages);
-    c.warps_per_block = warps;
-    c.stages = stages;
-    c.smem_bytes = kBarBytes + (size_t)warps * stages * St::kBytes;
-    c.stage_bytes = St::kBytes;
+    auto fit = [&](uint32_t reserve) {
+        WorkerConfig c{};
+        const int per = (int)St::kBytes + 8;                 // a stage and its mbarrier
+        const int usable = smem_budget - (int)reserve - 128;
+        int warps = usable / (2 * per);
+        warps = warps > kMaxWarps ? kMaxWarps : (warps < 1 ? 1 : warps);
+        int stages = usable / (warps * per);
+        stages = stages > kMaxStages ? kMaxStages : (stages < 2 ? 2 : stages);
+        c.warps_per_block = warps;
+        c.stages = stages;
+        c.stage_bytes = St::kBytes;
+        c.bars_off = reserve;
+        c.stages_off = (reserve + 8u * (uint32_t)(warps * stages) + 127u) & ~127u;
+        c.smem_bytes = c.stages_off + (size_t)warps * stages * St::kBytes;
+        return c;
+    };
+    if (!block_combine_fits<W, G>()) return fit(0);
+    WorkerConfig c = fit(block_part_bytes<W>() + 16u);
+    c.block_combine = 1;
+    c.bcnt_off = block_part_bytes<W>();
     return c;
 }
 
@@ -257,6 +347,12 @@ cudaError_t launch_wg(const WorkerArgs& a, int grid, cudaStream_t s, int smem_bu
     if ((int)c.smem_bytes > smem_budget) return cudaErrorInvalidConfiguration;
     WorkerArgs b = a;
     b.stages = c.stages;
+    b.bars_off = c.bars_off;
+    b.stages_off = c.stages_off;
+    b.bcnt_off = c.bcnt_off;
+    b.block_combine = a.interleave ? c.block_combine : 0;
+    // the block-level partial slots assume one range per block
+    if (b.block_combine && a.pt.P > grid) return cudaErrorInvalidConfiguration;
     if (a.interleave) return launch_pdl(k_worker<W, G, true>, grid, c.warps_per_block * 32, c.smem_bytes, s, b);
     return launch_pdl(k_worker<W, G, false>, grid, c.warps_per_block * 32, c.smem_bytes, s, b);
 }
