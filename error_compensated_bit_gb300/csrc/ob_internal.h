@@ -54,8 +54,7 @@ struct WorkerArgs {
     float b1, c1;
     int stages;             // pipeline stages per warp (set by the launcher)
     int interleave;         // 1: one range per block, warps interleaved; 0: one range per warp
-    int block_combine;      // interleaved: the block's warps pre-combine their partials (launcher)
-    uint32_t bars_off, stages_off, bcnt_off;   // dynamic shared-memory layout (launcher)
+    uint32_t bars_off, stages_off, bcnt_off;   // dynamic shared-memory layout (set by the launcher)
 };
 
 // Launch shape of the worker kernel for one (W, gradient type).

@@ -350,9 +350,8 @@ cudaError_t launch_wg(const WorkerArgs& a, int grid, cudaStream_t s, int smem_bu
     b.bars_off = c.bars_off;
     b.stages_off = c.stages_off;
     b.bcnt_off = c.bcnt_off;
-    b.block_combine = a.interleave ? c.block_combine : 0;
-    // the block-level partial slots assume one range per block
-    if (b.block_combine && a.pt.P > grid) return cudaErrorInvalidConfiguration;
+    // the block-level partial slots of the interleaved kernel assume one range per block
+    if (a.interleave && c.block_combine && a.pt.P > grid) return cudaErrorInvalidConfiguration;
     if (a.interleave) return launch_pdl(k_worker<W, G, true>, grid, c.warps_per_block * 32, c.smem_bytes, s, b);
     return launch_pdl(k_worker<W, G, false>, grid, c.warps_per_block * 32, c.smem_bytes, s, b);
 }
