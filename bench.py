@@ -456,7 +456,9 @@ def summarize(run, res, peak):
 
 
 # The workloads other than the headline, run in sequence after it (memory freed between):
-# (name, phase, workers or None for the recipe's, replayed from a CUDA graph)
+# (name, phase, workers or None for the recipe's, replayed from a CUDA graph[, chunk]).
+# The last two are the headline and LoCo buffers with 256-element chunks (the recipes
+# use chunk = n/W), the short-chunk paths of the worker and of LoCo.
 EXTRA_WORKLOADS = [
     ("bertB", "compressed", None, False), ("bertB", "warmup", None, False),
     ("sweep", "compressed", 2, False), ("sweep", "warmup", 2, False),
@@ -465,16 +467,20 @@ EXTRA_WORKLOADS = [
     ("sweep", "compressed", 16, False), ("sweep", "warmup", 16, False),
     ("loco", "loco", None, False), ("loco", "compressed", None, False),
     ("tiny", "compressed", None, False), ("tiny", "compressed", None, True),
+    ("bertL", "compressed", None, False, 256), ("loco", "loco", None, False, 256),
 ]
 
 
 def run_extra_workloads(torch, ob, synth, dev, steps, warmup, peak, only=None):
     out = {}
-    for name, phase, W, graph in EXTRA_WORKLOADS:
-        key = "%s%s_%s%s" % (name, "_W%d" % W if W else "", phase, "_graph" if graph else "")
+    for entry in EXTRA_WORKLOADS:
+        name, phase, W, graph = entry[:4]
+        chunk = entry[4] if len(entry) > 4 else None
+        key = "%s%s_%s%s%s" % (name, "_W%d" % W if W else "", phase, "_graph" if graph else "",
+                               "_c%d" % chunk if chunk else "")
         if only and not any(o in key for o in only):
             continue
-        wl = synth.workload(name, W=W)
+        wl = synth.workload(name, W=W, chunk=chunk)
         run = Run(torch, ob, synth, dev, wl, phase)
         n_steps = max(steps, 50) if name == "tiny" else steps
         res = run.measure(n_steps, warmup, graph=graph, clocks=ClockSampler(_gpu_index(dev)))

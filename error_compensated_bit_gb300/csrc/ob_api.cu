@@ -18,6 +18,10 @@ namespace {
 thread_local int g_last_cuda = 0;
 
 constexpr size_t kAlignWs = 256;
+// LoCo chunks up to this many elements take the one-pass absmax + quantize kernel: the
+// chunks its warps hold in flight together (a few tens of MB) stay in the L2 between
+// their two reads.
+constexpr int64_t kLocoOnePassMaxChunk = 4096;
 constexpr int kWarpsPerBlock = kBlock / 32;
 
 size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -50,6 +54,7 @@ struct ob_ctx {
     int grid_u = 0;             // update kernel: one resident wave
     int loco_occ_a[3] = {};     // resident blocks per SM of the LoCo absmax / quantize
     int loco_occ_q[3][2] = {};  // passes (per gradient type and code width; 0 = not asked)
+    int loco_occ_f[3][2] = {};  // the same for the one-pass short-chunk kernel
     Layout lay{};
     bool has_mask = false;
     int64_t launches = 0;
@@ -588,16 +593,25 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     a.eps = c->eps;
     a.lr = c->lr;
     a.wd = c->wd;
+    const int bi = bits == 4 ? 0 : 1;
+    const int grid = c->sms * 4;
+    if (c->C <= kLocoOnePassMaxChunk) {
+        // short chunks: absmax and quantize in one pass, each warp owning whole chunks
+        if (!c->loco_occ_f[dtype][bi]) c->loco_occ_f[dtype][bi] = occupancy_loco_fused(dtype, bits, c->C);
+        const int grid_f = c->sms * (c->loco_occ_f[dtype][bi] > 0 ? c->loco_occ_f[dtype][bi] : 2);
+        if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_fused(dtype, a, grid_f, s); })) return r;
+        if (int r = launch(c, OB_K_LOCO_SERVER, s, [&] { return launch_loco_server(a, grid, s); })) return r;
+        c->step += 1;
+        return OB_OK;
+    }
     const cudaError_t e = cudaMemsetAsync(a.amax_bits, 0, (size_t)c->W * c->nchunks * 4, s);
     if (e != cudaSuccess) return cuda_fail(e);
     // the absmax and quantize passes: one resident wave, each warp a contiguous range;
     // the server pass: four blocks per SM (its full wave), grid-stride
-    const int bi = bits == 4 ? 0 : 1;
     if (!c->loco_occ_a[dtype]) c->loco_occ_a[dtype] = occupancy_loco_absmax(dtype);
     if (!c->loco_occ_q[dtype][bi]) c->loco_occ_q[dtype][bi] = occupancy_loco_quant(dtype, bits);
     const int grid_a = c->sms * (c->loco_occ_a[dtype] > 0 ? c->loco_occ_a[dtype] : 2);
     const int grid_q = c->sms * (c->loco_occ_q[dtype][bi] > 0 ? c->loco_occ_q[dtype][bi] : 2);
-    const int grid = c->sms * 4;
     if (int r = launch(c, OB_K_LOCO_ABSMAX, s, [&] { return launch_loco_absmax(dtype, a, grid_a, s); })) return r;
     if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_quant(dtype, a, grid_q, s); })) return r;
     if (int r = launch(c, OB_K_LOCO_SERVER, s, [&] { return launch_loco_server(a, grid, s); })) return r;

@@ -57,6 +57,15 @@ __device__ __forceinline__ void ld8_stream(const float* p, float (&v)[8])
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// The same 8 floats cached in the L2 only (for data read again soon).
+__device__ __forceinline__ void ld8_l2(const float* p, float (&v)[8])
+{
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 __device__ __forceinline__ void st8_stream(float* p, const float (&v)[8])
 {
     __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
@@ -116,6 +125,11 @@ struct GradRaw {
     {
         return GradRaw{__ldcs(reinterpret_cast<const uint4*>(static_cast<const G*>(base) + idx))};
     }
+    // the same load kept in the L2 (read again soon)
+    static __device__ __forceinline__ GradRaw load_l2(const void* base, int64_t idx)
+    {
+        return GradRaw{__ldcg(reinterpret_cast<const uint4*>(static_cast<const G*>(base) + idx))};
+    }
     __device__ __forceinline__ void widen(float (&v)[8]) const;
 };
 
@@ -126,6 +140,11 @@ struct GradRaw<float> {
     {
         const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
         return GradRaw{__ldcs(p), __ldcs(p + 1)};
+    }
+    static __device__ __forceinline__ GradRaw load_l2(const void* base, int64_t idx)
+    {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
+        return GradRaw{__ldcg(p), __ldcg(p + 1)};
     }
     __device__ __forceinline__ void widen(float (&v)[8]) const
     {

@@ -157,12 +157,14 @@ cudaError_t launch_export(const ExportArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_absmax(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_loco_fused(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 
 // Resident blocks per SM of the server kernel for W / of the update kernel; 0 on error.
 int occupancy_server(int W);
 int occupancy_update();
 int occupancy_loco_absmax(int dtype);
 int occupancy_loco_quant(int dtype, int bits);
+int occupancy_loco_fused(int dtype, int bits, int64_t C);
 
 // Launch `kernel` with the programmatic stream-serialization attribute (see pdl_wait in
 // ob_tma.cuh): it may begin while the previous kernel on the stream finishes.

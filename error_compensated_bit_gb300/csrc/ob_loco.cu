@@ -181,6 +181,147 @@ __global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
     }
 }
 
+// Absmax and quantization in one kernel, for chunks short enough that a warp owns whole
+// ones: the (row, chunk) slots -- slot w*nchunks + k covers elements [slot*C, (slot+1)*C)
+// of the flat [W][n] arrays -- are split into contiguous ranges per warp. Each slot is
+// read twice, first for its absmax (kept in the L2, as the slots the warps hold in flight
+// together stay well inside it) and straight after to quantize, so DRAM sees the
+// gradients and errors once. Scale, codes and errors are those of the two-pass form
+// exactly: the same maximum (the warp's maximum of |c| is the chunk's) and the same
+// quantize8.
+constexpr int kLocoOnePassU = 2;     // groups in flight per sweep (both sweeps share registers)
+
+template <typename G, int BITS>
+__global__ void __launch_bounds__(kBlock) k_loco_fused(LocoArgs a)
+{
+    constexpr int U = kLocoOnePassU;
+    const int lane = threadIdx.x & 31;
+    const float L = (float)((1 << (BITS - 1)) - 1);
+    int64_t s0, s1;
+    warp_items((int64_t)a.W * a.nchunks, s0, s1);
+    const int64_t CG = a.C / 256;
+    for (int64_t slot = s0; slot < s1; ++slot) {
+        const int64_t t0 = slot * CG;
+        float run = 0.0f;
+        for (int64_t tb = 0; tb < CG; tb += U) {
+            GradRaw<G> gr[U];
+            float ev[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (tb + u < CG) {
+                    const int64_t e0 = (t0 + tb + u) * 256 + lane * 8;
+                    gr[u] = GradRaw<G>::load_l2(a.g, e0);
+                    ld8_l2(a.err + e0, ev[u]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (tb + u < CG) {
+                    float gv[8];
+                    gr[u].widen(gv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) run = fmaxf(run, fabsf(__fadd_rn(gv[j], __fmul_rn(a.ratio, ev[u][j]))));
+                }
+            }
+        }
+        const float s = __fdiv_rn(warp_max(run), L);
+        const float inv = __frcp_rn(s);
+        if (lane == 0) a.scale[slot] = s;
+        for (int64_t tb = 0; tb < CG; tb += U) {
+            GradRaw<G> gr[U];
+            float ev[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (tb + u < CG) {
+                    const int64_t e0 = (t0 + tb + u) * 256 + lane * 8;
+                    gr[u] = GradRaw<G>::load(a.g, e0);
+                    ld8_stream(a.err + e0, ev[u]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (tb + u < CG) {
+                    float gv[8];
+                    gr[u].widen(gv);
+                    uint32_t lo, hi;
+                    quantize8<BITS>(gv, ev[u], s, inv, a.ratio, a.beta, a.keep, lo, hi);
+                    const int64_t e0 = (t0 + tb + u) * 256 + lane * 8;
+                    st8_stream(a.err + e0, ev[u]);
+                    uint8_t* out = a.codes + e0 * BITS / 8;
+                    if (BITS == 4) __stcs(reinterpret_cast<unsigned int*>(out), lo);
+                    else __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
+                }
+            }
+        }
+    }
+}
+
+// The same for chunks of one, two or four groups (C = 256, 512, 1024): each warp takes
+// kLocoU groups at a time -- whole chunks, as the chunk size divides kLocoU groups and a
+// warp's range starts on a chunk -- and keeps them in registers: the maxima of the
+// groups, combined per chunk, give the scales, and the groups are quantized from the
+// registers they were loaded into. One read, and kLocoU groups in flight per warp.
+// Residency (measured): three blocks per SM for 16-bit gradients (80 registers), two for
+// float32 ones, whose wider rows spill at 80.
+template <typename G, int BITS>
+__global__ void __launch_bounds__(kBlock, sizeof(G) == 4 ? 2 : 3) k_loco_fused_small(LocoArgs a)
+{
+    constexpr int U = kLocoU;
+    const int lane = threadIdx.x & 31;
+    const float L = (float)((1 << (BITS - 1)) - 1);
+    int64_t s0, s1;
+    warp_items((int64_t)a.W * a.nchunks, s0, s1);
+    const int CG = (int)(a.C / 256);                  // 1, 2 or 4
+    const int64_t t1 = s1 * CG;
+    for (int64_t tb = s0 * CG; tb < t1; tb += U) {
+        GradRaw<G> gr[U];
+        float ev[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (tb + u < t1) {
+                const int64_t e0 = (tb + u) * 256 + lane * 8;
+                gr[u] = GradRaw<G>::load(a.g, e0);
+                ld8_stream(a.err + e0, ev[u]);
+            }
+        }
+        float mx[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float run = 0.0f;
+            if (tb + u < t1) {
+                float gv[8];
+                gr[u].widen(gv);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) run = fmaxf(run, fabsf(__fadd_rn(gv[j], __fmul_rn(a.ratio, ev[u][j]))));
+            }
+            mx[u] = warp_max(run);
+        }
+        // the maximum of each group's chunk (groups u..u+CG-1 with u a multiple of CG)
+        if (CG >= 2) {
+#pragma unroll
+            for (int u = 0; u < U; u += 2) mx[u] = mx[u + 1] = fmaxf(mx[u], mx[u + 1]);
+        }
+        if (CG == 4) mx[0] = mx[1] = mx[2] = mx[3] = fmaxf(mx[0], mx[2]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (tb + u < t1) {
+                const float sc = __fdiv_rn(mx[u], L);
+                const float inv = __frcp_rn(sc);
+                if (lane == 0 && (u % CG) == 0) a.scale[(tb + u) / CG] = sc;
+                float gv[8];
+                gr[u].widen(gv);
+                uint32_t lo, hi;
+                quantize8<BITS>(gv, ev[u], sc, inv, a.ratio, a.beta, a.keep, lo, hi);
+                const int64_t e0 = (tb + u) * 256 + lane * 8;
+                st8_stream(a.err + e0, ev[u]);
+                uint8_t* out = a.codes + e0 * BITS / 8;
+                if (BITS == 4) __stcs(reinterpret_cast<unsigned int*>(out), lo);
+                else __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
+            }
+        }
+    }
+}
+
 template <int BITS>
 __device__ __forceinline__ void load_codes(const uint8_t* p, int (&q)[8])
 {
@@ -284,6 +425,42 @@ int occupancy_loco_quant(int dtype, int bits)
     if (dtype == 0) return occ_of(k_loco_quant<float, 8>);
     if (dtype == 1) return occ_of(k_loco_quant<__half, 8>);
     return occ_of(k_loco_quant<__nv_bfloat16, 8>);
+}
+
+cudaError_t launch_loco_fused(int dtype, const LocoArgs& a, int grid, cudaStream_t s)
+{
+    const bool small = a.C <= 256 * kLocoU;
+#define OB_LOCO_FUSED(G, B)                                              \
+    do {                                                                 \
+        if (small) k_loco_fused_small<G, B><<<grid, kBlock, 0, s>>>(a);  \
+        else k_loco_fused<G, B><<<grid, kBlock, 0, s>>>(a);              \
+    } while (0)
+    if (a.bits == 4) {
+        if (dtype == 0) OB_LOCO_FUSED(float, 4);
+        else if (dtype == 1) OB_LOCO_FUSED(__half, 4);
+        else OB_LOCO_FUSED(__nv_bfloat16, 4);
+    } else {
+        if (dtype == 0) OB_LOCO_FUSED(float, 8);
+        else if (dtype == 1) OB_LOCO_FUSED(__half, 8);
+        else OB_LOCO_FUSED(__nv_bfloat16, 8);
+    }
+#undef OB_LOCO_FUSED
+    return cudaGetLastError();
+}
+
+int occupancy_loco_fused(int dtype, int bits, int64_t C)
+{
+    const bool small = C <= 256 * kLocoU;
+#define OB_LOCO_OCC(G, B) return small ? occ_of(k_loco_fused_small<G, B>) : occ_of(k_loco_fused<G, B>)
+    if (bits == 4) {
+        if (dtype == 0) OB_LOCO_OCC(float, 4);
+        if (dtype == 1) OB_LOCO_OCC(__half, 4);
+        OB_LOCO_OCC(__nv_bfloat16, 4);
+    }
+    if (dtype == 0) OB_LOCO_OCC(float, 8);
+    if (dtype == 1) OB_LOCO_OCC(__half, 8);
+    OB_LOCO_OCC(__nv_bfloat16, 8);
+#undef OB_LOCO_OCC
 }
 
 cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s)

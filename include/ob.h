@@ -196,6 +196,9 @@ int ob_compressed_step_host(ob_ctx *ctx, const void *grads_host, void *grads_dev
  * frozen). bits is 4 (two codes per byte, even element in the low nibble, two's
  * complement) or 8 (one signed byte). loco_err [W][n] float holds e~ (zero at start).
  * loco_ws must hold ob_loco_workspace_bytes(ctx, bits) bytes, zeroed before first use.
+ * Chunks of up to 4096 elements are quantized in one pass that also finds their absmax
+ * (profiled as OB_K_LOCO_QUANT; OB_K_LOCO_ABSMAX then records no launch); longer chunks
+ * take a separate absmax pass first. The results are the same either way.
  */
 int ob_loco_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m, float *v,
                  float *loco_err, float beta, int bits, void *loco_ws, void *stream);

@@ -77,7 +77,7 @@ def test_dominant_kernel_bytes(bench):
 
 
 def test_extra_workloads_cover_every_recipe(bench):
-    keys = {(name, phase, W) for name, phase, W, _ in bench.EXTRA_WORKLOADS}
+    keys = {tuple(e[:3]) for e in bench.EXTRA_WORKLOADS}
     assert ("bertB", "compressed", None) in keys
     for W in (2, 4, 8, 16):
         assert ("sweep", "compressed", W) in keys and ("sweep", "warmup", W) in keys

@@ -20,7 +20,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 # (workload, W, phase, chunk): chunk None is the workload's own (n/W); the short chunks
 # run the worker with one range per warp, scales written by their only contributor and
-# the separate scale-copy kernel.
+# the separate scale-copy kernel, and LoCo's one-pass absmax + quantize kernels.
 CASES = [
     ("bertL", 8, "compressed", None),
     ("bertL", 8, "compressed", 2048),
@@ -30,6 +30,8 @@ CASES = [
     ("sweep", 16, "compressed", 256),
     ("loco", 4, "loco", None),
     ("loco", 4, "compressed", None),
+    ("loco", 4, "loco", 256),        # one-pass LoCo, chunks held in registers
+    ("sweep", 4, "loco", 2048),      # one-pass LoCo, chunks read twice through the L2
 ]
 
 
@@ -73,7 +75,8 @@ def test_full_size_sampled_chunks(ora, name, W, phase, chunk):
         lws = torch.zeros(ctx.loco_workspace_bytes(4), dtype=torch.uint8, device=dev)
     g = torch.empty(W, n, dtype=wl.grad_dtype, device=dev)
 
-    picks = [0, nch - 1] if n < 10 ** 9 else [nch - 1]     # keep the oracle's share bounded
+    # keep the oracle's share bounded: short chunks are cheap, so three are checked
+    picks = [0, nch // 2, nch - 1] if C <= 4096 else ([0, nch - 1] if n < 10 ** 9 else [nch - 1])
     sl = {k: slice(k * C, (k + 1) * C) for k in picks}
     host = lambda t, k: t[sl[k]].cpu().numpy()
     states = {}
