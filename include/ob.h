@@ -93,8 +93,9 @@ enum {
  * Create a context for an n-element buffer, W workers and `chunk` elements per scale,
  * with Adam's b1, b2, eps and the learning rate lr (weight decay 0, bias correction
  * off, as in the tutorial page's BERT configurations, §6.2). Queries the current
- * device and, when there is one, opts the worker kernels into the dynamic shared memory
- * they launch with on that device (OB_ECUDA if that fails); allocates host memory only.
+ * device and, when there is one, opts the worker and server kernels into the dynamic
+ * shared memory they launch with on that device (OB_ECUDA if that fails); allocates host
+ * memory only.
  * Contexts on different devices, or used from different host threads, are independent.
  * Returns OB_EINVAL for sizes outside the rules above or non-finite hyper-parameters;
  * *out is set only on OB_OK.
@@ -165,7 +166,10 @@ int ob_warmup_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m
  *   all:       m = T_k*sign(y) [* mask];  x -= lr*(m/(sqrt(v)+eps) [+wd*x])
  * Three kernels on the stream: worker compress, server average/recompress, update; a
  * fourth (OB_K_SCALES) moves the step's chunk scales into the "previous" slots when
- * they are more than 4096 (short chunks), which the update does itself otherwise.
+ * they are more than 4096 (short chunks), which the update does itself otherwise. They
+ * are launched with programmatic dependent launch: each may be scheduled while the
+ * kernel before it on the stream finishes, and waits for it before touching memory, so
+ * stream order holds as for ordinary launches.
  */
 int ob_compressed_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m,
                        const float *v, float *worker_err, float *server_err, void *ws,
