@@ -68,6 +68,18 @@ CASES = [
     (16, "f32", 173, 173),
     (16, "bf16", 96, 8),
     (7, "f16", 2000, 400),
+    # short chunks with block ranges spanning many chunks: one range per warp, the chunks
+    # inside a warp's range scaled by that warp alone (row counts padded to 2, 4, 8, 16)
+    (1, "f32", 1000, 1),
+    (2, "bf16", 10000, 2),
+    (3, "f16", 6000, 2),
+    (6, "f32", 700, 1),
+    (9, "bf16", 500, 1),
+    (11, "f16", 400, 1),
+    (13, "f32", 1500, 2),
+    # 16-bit gradients with W >= 11 and long chunks: the interleaved worker without the
+    # block-level pre-combination of partials
+    (12, "f16", 300, 300),
 ]
 
 
@@ -115,7 +127,9 @@ def test_edge_cases(ora, case, C):
     that warp alone). Degenerate chunks -- all zero, subnormal, or sums of squares that
     overflow float32 -- take the double-precision fallback in both."""
     rng = np.random.default_rng(5)
-    W, n = 4, 4 * 256 * 64
+    # with 256-element chunks the buffer is long enough that a block's range spans many
+    # chunks, so the worker runs one range per warp (at 64 groups per row it would not)
+    W, n = 4, 4 * 256 * (1024 if C == 256 else 64)
     mask = None
     st = random_state(rng, n, W, C)
     g = np.zeros((W, n), np.float32)
