@@ -467,7 +467,8 @@ __device__ __forceinline__ void flush_rest(const Part& pt, int wpr, int64_t k, d
                                            float* scale_out, int64_t C, const float* rows, int64_t row_stride,
                                            int lane)
 {
-    __threadfence();
+    __threadfence();                // every lane's stores (partials, rows) before ...
+    __syncwarp();                   // ... lane 0 counts this contributor in
     unsigned last = 0;
     if (lane == 0) {
         int64_t lo, hi;
@@ -545,6 +546,7 @@ __device__ __forceinline__ void flush_chunk(const Part& pt, int64_t q, int wpr, 
         flush_rest_outlined<R>(pt, wpr, k, part, cnt, scale_out, C, rows, row_stride, lane);
     } else {
         __threadfence();
+        __syncwarp();
         unsigned last = 0;
         if (lane == 0) {
             int64_t lo, hi;

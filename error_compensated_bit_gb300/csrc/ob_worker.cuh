@@ -88,6 +88,9 @@ __device__ __noinline__ void block_flush(const Part& pt, int64_t q, int wpb, int
         for (int w = 0; w < wpb; ++w) sum += bpart[(j * kMaxWarps + w) * W + r];
         part[((int64_t)r * pt.P + q) * pt.J + j] = sum;
     }
+    // lanes 0..W-1 wrote the block's partials; each makes its own writes visible before
+    // lane 0 counts the range in (in flush_rest)
+    __threadfence();
     __syncwarp();
     flush_rest<W>(pt, 1, k, part, cnt, scale_out, C, rows, row_stride, lane);
 }
