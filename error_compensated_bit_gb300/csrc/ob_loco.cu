@@ -8,15 +8,18 @@
 // compression, then synchronise), key design item 2 (the proportion of the compensation
 // is tuned: `ratio`, 1 by default) and the abstract (compatible with Adam).
 //
-// Three passes. The absmax of c = g + e~ over a chunk must be known before any element
-// of the chunk can be quantized, and a chunk spans up to n/W elements, so c is formed
-// twice (pass 1 for the absmax, pass 2 to quantize) instead of being stored.
-//   pass 1  amax[w][k] = max |c|, c = g + ratio*e~     (atomicMax on float bits: exact)
+// Three passes for long chunks. The absmax of c = g + ratio*e~ over a chunk must be known
+// before any element of the chunk can be quantized, and a chunk spans up to n/W
+// elements, so c is formed twice (pass 1 for the absmax, pass 2 to quantize) instead of
+// being stored.
+//   pass 1  amax[w][k] = max |c|                         (atomicMax on float bits: exact)
 //   pass 2  s = amax/L; q = clamp(rint(c/s), -L, L) (0 when s = 0); e = c - q*s;
 //           e~ = beta*e~ + (1-beta)*e; codes <- q
 //   pass 3  gbar = (sum over w of q_w*s_w)/W; Adam on m, v, x
 // Memory per element: pass 1 W*(grad+4), pass 2 W*(grad+8+bits/8), pass 3
-// W*bits/8 + 24.
+// W*bits/8 + 24. Chunks of up to 4096 elements take passes 1 and 2 in one kernel whose
+// warps own whole chunks (k_loco_fused_small, k_loco_fused), reading the gradients and
+// errors from DRAM once.
 #include "ob_common.cuh"
 #include "ob_div.cuh"
 

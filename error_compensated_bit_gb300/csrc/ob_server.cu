@@ -153,8 +153,8 @@ struct ServerStage {
 template <int W>
 __global__ void __launch_bounds__(kBlock, 4) k_server_staged(ServerArgs a)
 {
+    static_assert(W > 8, "the staged server pass covers more than eight workers");
     using St = ServerStage<W>;
-    constexpr int T = W < 8 ? W : 8;     // workers covered by the table
     constexpr int S = St::kStages;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kBlock, 4) k_server_staged(ServerArgs a)
 
         for (int64_t gi = g0; gi < g1; ++gi) {
             if (gi == kend) {
-                flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+                flush_chunk<1, kFlushLastCall>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
                 ++k;
                 kend += pt.CG;
 #pragma unroll
@@ -227,26 +227,23 @@ __global__ void __launch_bounds__(kBlock, 4) k_server_staged(ServerArgs a)
             // byte (lane & 3) of word (lane >> 2) of each row: this lane's 8 sign bits
             uint64_t lo = 0, hi = 0;
 #pragma unroll
-            for (int w = 0; w < T; ++w) lo |= (uint64_t)stg[St::kSignOff + w * 32 + lane] << (8 * w);
-            if (W > 8) {
+            for (int w = 0; w < 8; ++w) lo |= (uint64_t)stg[St::kSignOff + w * 32 + lane] << (8 * w);
 #pragma unroll
-                for (int w = 8; w < W; ++w) hi |= (uint64_t)stg[St::kSignOff + w * 32 + lane] << (8 * (w - 8));
-            }
+            for (int w = 8; w < W; ++w) hi |= (uint64_t)stg[St::kSignOff + w * 32 + lane] << (8 * (w - 8));
             __syncwarp();                   // every lane is done with stage s
             if (gi + S < g1) issue(s, gi + S);
             cp_async_commit();
             lo = transpose8x8(lo);
-            if (W > 8) hi = transpose8x8(hi);
+            hi = transpose8x8(hi);
             uint32_t byte = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
+                // the table's partial sum over workers 0..7, then workers 8.. in order
                 float avg = tab[(uint32_t)(lo >> (8 * j)) & 0xffu];
-                if (W > 8) {
-                    const uint32_t pat = (uint32_t)(hi >> (8 * j)) & 0xffu;
+                const uint32_t pat = (uint32_t)(hi >> (8 * j)) & 0xffu;
 #pragma unroll
-                    for (int w = 8; w < W; ++w) avg = __fadd_rn(avg, signed_scale(sw[w], (pat >> (w - 8)) & 1u));
-                    avg = (W & (W - 1)) == 0 ? __fmul_rn(avg, 1.0f / (float)W) : __fdiv_rn(avg, (float)W);
-                }
+                for (int w = 8; w < W; ++w) avg = __fadd_rn(avg, signed_scale(sw[w], (pat >> (w - 8)) & 1u));
+                avg = (W & (W - 1)) == 0 ? __fmul_rn(avg, 1.0f / (float)W) : __fdiv_rn(avg, (float)W);
                 const float es = __fsub_rn(yv[j], signed_scale(tp, yv[j] >= 0.0f));
                 const float y = __fadd_rn(avg, es);
                 yv[j] = y;
@@ -258,7 +255,7 @@ __global__ void __launch_bounds__(kBlock, 4) k_server_staged(ServerArgs a)
             if ((lane & 3) == 0) __stcs(a.sbits + gi * 8 + (lane >> 2), word);
         }
         cp_async_wait<0>();                 // nothing of this range is left in flight
-        flush_chunk<1, (W > 8 ? kFlushLastCall : kFlushInline)>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
+        flush_chunk<1, kFlushLastCall>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
 }
 
