@@ -259,9 +259,9 @@ __global__ void __launch_bounds__(kBlock) k_loco_fused(LocoArgs a)
     }
 }
 
-// The same for chunks of one, two or four groups (C = 256, 512, 1024): each warp takes
-// kLocoU groups at a time -- whole chunks, as the chunk size divides kLocoU groups and a
-// warp's range starts on a chunk -- and keeps them in registers: the maxima of the
+// The same for chunks of one, two or four groups (C = 256, 512, 1024; not 768): each warp
+// takes kLocoU groups at a time -- whole chunks, as the chunk size divides kLocoU groups
+// and a warp's range starts on a chunk -- and keeps them in registers: the maxima of the
 // groups, combined per chunk, give the scales, and the groups are quantized from the
 // registers they were loaded into. One read, and kLocoU groups in flight per warp.
 // Residency (measured): three blocks per SM for 16-bit gradients (80 registers), two for
@@ -430,9 +430,18 @@ int occupancy_loco_quant(int dtype, int bits)
     return occ_of(k_loco_quant<__nv_bfloat16, 8>);
 }
 
+// The register kernel needs the chunk's group count to divide kLocoU (1, 2 or 4 groups):
+// its blocks of kLocoU groups then hold whole chunks. Other short chunks (3 groups, or 5 to
+// 16) take the two-sweep kernel.
+static bool loco_small_chunks(int64_t C)
+{
+    const int64_t cg = C / 256;
+    return cg == 1 || cg == 2 || cg == 4;
+}
+
 cudaError_t launch_loco_fused(int dtype, const LocoArgs& a, int grid, cudaStream_t s)
 {
-    const bool small = a.C <= 256 * kLocoU;
+    const bool small = loco_small_chunks(a.C);
 #define OB_LOCO_FUSED(G, B)                                              \
     do {                                                                 \
         if (small) k_loco_fused_small<G, B><<<grid, kBlock, 0, s>>>(a);  \
@@ -453,7 +462,7 @@ cudaError_t launch_loco_fused(int dtype, const LocoArgs& a, int grid, cudaStream
 
 int occupancy_loco_fused(int dtype, int bits, int64_t C)
 {
-    const bool small = C <= 256 * kLocoU;
+    const bool small = loco_small_chunks(C);
 #define OB_LOCO_OCC(G, B) return small ? occ_of(k_loco_fused_small<G, B>) : occ_of(k_loco_fused<G, B>)
     if (bits == 4) {
         if (dtype == 0) OB_LOCO_OCC(float, 4);

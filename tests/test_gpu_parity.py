@@ -247,16 +247,18 @@ def test_warmup_then_compressed(ora):
     (4, "bf16", 4, 2, 1.0), (2, "f32", 8, 2, 1.0), (3, "f16", 4, 2, 1.0),
     (4, "bf16", 4, 400, 1.0), (2, "f32", 8, 25, 1.0),
     (4, "bf16", 4, 2, 0.5), (3, "f16", 8, 25, 0.0), (2, "f32", 4, 400, 0.3),
-    (2, "bf16", 4, 200, 1.0), (3, "f32", 8, 100, 0.5)])
+    (2, "bf16", 4, 200, 1.0), (3, "f32", 8, 100, 0.5), (2, "f16", 4, 400 // 3, 1.0)])
 def test_loco_parity(ora, W, dtype, bits, per_row, ratio):
     """per_row chunks per worker row: 400, 200 and 100 make chunks of one, two and four
-    256-element groups (quantized in one pass from registers), 25 chunks of 4096 elements
-    (one pass, read twice through the L2), 2 long chunks (separate absmax pass). ratio:
+    256-element groups (quantized in one pass from registers), 133 chunks of three groups
+    and 25 chunks of 4096 elements (one pass, read twice through the L2), 2 long chunks
+    (separate absmax pass). ratio:
     the share of the averaged error compensated into the gradient (1 is plain
     c = g + e~)."""
     from error_compensated_bit_gb300 import ob
     rng = np.random.default_rng(40 + W + per_row + int(ratio * 10))
-    n = W * 256 * 400
+    groups = 399 if per_row == 400 // 3 else 400      # 133 chunks of three groups
+    n = W * 256 * groups
     C = n // W // per_row
     st = random_state(rng, n, W, C)
     st.v[:] = 0.0
