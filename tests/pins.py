@@ -415,6 +415,34 @@ def pin_loco_codes(ora):
     np.testing.assert_allclose(st.x, want, rtol=2e-6, atol=1e-30)
 
 
+def pin_loco_codes_8bit(ora):
+    """8-bit codes: the levels are -127..127 (L = 2^7 - 1) and each code is one signed
+    byte in element order. Inputs that are exact multiples of a power-of-two step with the
+    largest magnitude 127 steps give exactly those levels, zero error, and scale = step."""
+    n, W, C = 256, 1, 256
+    q = np.concatenate([np.arange(-127, 128), [0]]).astype(np.float32)
+    s = np.float32(2.0 ** -12)
+    g = (q * s).reshape(1, n)
+    st = O.OracleState(n, W, C, x=np.zeros(n), m=np.zeros(n), v=np.zeros(n), lr=1e-4)
+    err = np.zeros((W, n), np.float32)
+    out = ora.loco_step(st, g, err, beta=0.0, bits=8)
+    assert np.array_equal(out["scales"], _f32([[s]]))
+    assert np.array_equal(out["codes"][0].view(np.int8), q.astype(np.int8))
+    assert not err.any()
+    # above 127 steps the codes clamp: one element at 254 steps makes the step twice as
+    # large, so level 127 now stands for 254 steps and odd multiples round to even ones
+    g2 = g.copy()
+    g2[0, 0] = np.float32(254) * s
+    err = np.zeros((W, n), np.float32)
+    out2 = ora.loco_step(O.OracleState(n, W, C, x=np.zeros(n), m=np.zeros(n), v=np.zeros(n), lr=1e-4),
+                         g2, err, beta=0.0, bits=8)
+    assert np.array_equal(out2["scales"], _f32([[2 * s]]))
+    codes = out2["codes"][0].view(np.int8).astype(np.int32)
+    assert codes[0] == 127
+    halves = q[1:].astype(np.float64) / 2            # the other elements in units of 2s
+    assert np.array_equal(codes[1:], np.rint(halves).astype(np.int32))   # ties to even
+
+
 def pin_loco_error_bound(ora):
     rng = np.random.default_rng(31)
     n, W, C = 4096, 2, 512

@@ -48,6 +48,10 @@ MUTANTS = [
      "c[i] = ora_grad(grads, dtype, (int64_t)w * n + i) + comp;",
      "c[i] = ora_grad(grads, dtype, (int64_t)w * n + i);", 0),
     ("loco_ratio_ignored", "float comp = ratio * et[i];", "float comp = et[i];", 0),
+    ("loco_8bit_codes_shifted", "for (int64_t i = 0; i < n; ++i) cw[i] = (uint8_t)qw[i];",
+     "for (int64_t i = 0; i < n; ++i) cw[i] = (uint8_t)(qw[i] + 1);", 0),
+    ("loco_levels_off_by_one", "const int levels = (1 << (bits - 1)) - 1;",
+     "const int levels = bits == 8 ? 128 : (1 << (bits - 1)) - 1;", 0),
     ("loco_ratio_on_average", "float old_part = beta * et[i];", "float old_part = beta * ratio * et[i];", 0),
 ]
 
