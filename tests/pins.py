@@ -18,15 +18,17 @@ What pins what:
                     arithmetic (every intermediate is a small dyadic rational)
   identity_sgd      with the compressor replaced by the identity the compressed step is
                     momentum SGD preconditioned by the frozen variance:
-                    torch.optim.SGD on g / (sqrt(v) + eps)
+                    torch.optim.SGD on g / (sqrt(v) + eps), with the weight decay applied
+                    to the parameters before the step (decoupled, as AdamW does)
   w1_server         with one worker the server stage reproduces the worker's message
   mask              masked momentum is exactly zero; unmasked values match the unmasked
                     run; errors are not masked
   warmup_adamw      the warm-up step is AdamW on the mean gradient (torch.optim.AdamW),
                     and from zero state it has the closed form -lr*c1*g/(sqrt(c2)|g|+eps)
   comm_bytes        the pages' 32x (97%) and "up to 5x" communication figures
-  loco_*            LoCo codes for exactly representable inputs, nibble layout, the
-                    half-step error bound, the moving average's closed form, the
+  loco_*            LoCo codes for exactly representable inputs, nibble layout, 8-bit
+                    codes as signed bytes (clamping, ties to even), the half-step error
+                    bound, the moving average's closed form, the
                     dequantized mean driving a first Adam step (closed form); the
                     compensation ratio: a case worked by hand in dyadic arithmetic at
                     ratio 1/2 (ties to even included), and ratio 0 making the codes,
@@ -280,11 +282,13 @@ def _rand_state(rng, n, W, C, **kw):
 
 
 def pin_identity_sgd(ora):
-    """Identity compressor: momentum SGD (torch.optim.SGD) on g / (sqrt(v) + eps)."""
+    """Identity compressor: momentum SGD (torch.optim.SGD) on g / (sqrt(v) + eps); with a
+    weight decay wd, the parameters are first scaled by (1 - lr*wd) (decoupled decay, as
+    AdamW applies it), so the step is x - lr*(m/(sqrt(v)+eps) + wd*x)."""
     rng = np.random.default_rng(21)
-    for W in (1, 3):
+    for W, wd in ((1, 0.0), (3, 0.0), (2, 0.01)):
         n, C = 1024, 256
-        st = _rand_state(rng, n, W, C, b1=0.9, eps=1e-8, lr=1e-3)
+        st = _rand_state(rng, n, W, C, b1=0.9, eps=1e-8, lr=1e-3, wd=wd)
         p = torch.nn.Parameter(torch.from_numpy(st.x.copy()).double())
         f = lambda a: float(np.float32(a))
         opt = torch.optim.SGD([p], lr=f(1e-3), momentum=f(0.9), dampening=f(0.9))
@@ -294,6 +298,8 @@ def pin_identity_sgd(ora):
             g = (rng.standard_normal((W, n)) * 1e-3).astype(np.float32)
             ora.compressed_step(st, g, identity=True)
             p.grad = torch.from_numpy(g.astype(np.float64).mean(0)) / precond
+            with torch.no_grad():
+                p.mul_(1.0 - f(1e-3) * f(wd))
             opt.step()
             assert not st.ew.any() and not st.es.any()
             np.testing.assert_allclose(st.x, p.detach().numpy(), rtol=1e-5, atol=1e-7)

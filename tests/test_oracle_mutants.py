@@ -38,6 +38,8 @@ MUTANTS = [
     ("warmup_v_not_squared", "float v_new = c2 * sq;", "float v_new = c2 * gbar;", 0),
     ("warmup_mean_not_divided", "float gbar = acc / (float)W;", "float gbar = acc;", 0),
     ("weight_decay_sign", "u = u + decay;", "u = u - decay;", 0),
+    ("compressed_drops_weight_decay", "x[i] = ora_apply_update(x[i], mi, v[i], eps, lr, wd);",
+     "x[i] = ora_apply_update(x[i], mi, v[i], eps, lr, 0.0f);", 0),
     ("loco_truncate", "float r = rintf(c[i] / s);", "float r = truncf(c[i] / s);", 0),
     ("loco_nibbles_swapped",
      "cw[j] = (uint8_t)(((uint8_t)qw[2 * j] & 0x0f) | (((uint8_t)qw[2 * j + 1] & 0x0f) << 4));",
