@@ -29,7 +29,9 @@ What pins what:
   loco_*            LoCo codes for exactly representable inputs, nibble layout, 8-bit
                     codes as signed bytes (clamping, ties to even), the half-step error
                     bound, the moving average's closed form, the
-                    dequantized mean driving a first Adam step (closed form); the
+                    dequantized mean driving a first Adam step (closed form), and with
+                    exactly quantizable gradients the Adam part equal to the warm-up
+                    step (itself pinned to AdamW) from non-zero state; the
                     compensation ratio: a case worked by hand in dyadic arithmetic at
                     ratio 1/2 (ties to even included), and ratio 0 making the codes,
                     scales and (beta = 0) new errors independent of the old errors
@@ -529,6 +531,31 @@ def pin_loco_ratio_zero(ora):
         assert np.array_equal(e, errs[0])
     amax = np.abs(g).reshape(W, -1, C).max(2)
     np.testing.assert_allclose(outs[0]["scales"], amax / 7, rtol=1e-7)
+
+
+def pin_loco_adam_is_the_warmup_step(ora):
+    """With gradients that quantize exactly (every chunk has a level of +-7 steps and its
+    own power-of-two step, so c = q*s with zero error and e~ stays zero), the dequantized
+    mean equals the plain mean and the LoCo step's Adam part must equal the warm-up step
+    (pinned against torch.optim.AdamW) bit for bit, from non-zero m and v, step after
+    step: the same b1, b2, chunk-by-chunk scales and update."""
+    rng = np.random.default_rng(88)
+    n, W, C = 1024, 2, 256
+    st_l = _rand_state(rng, n, W, C, b1=0.9, b2=0.999, eps=1e-8, lr=1e-3)
+    st_l.m[:] = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    st_w = st_l.copy()
+    err = np.zeros((W, n), np.float32)
+    for step in range(3):
+        q = rng.integers(-7, 8, (W, n)).astype(np.float32)
+        q[:, ::C] = rng.choice([-7.0, 7.0], (W, n // C))                # a +-7 in every chunk
+        steps = np.float32(2.0) ** rng.integers(-14, -8, (W, n // C)).astype(np.float32)
+        g = (q * np.repeat(steps, C, axis=1)).astype(np.float32)
+        out = ora.loco_step(st_l, g, err, beta=0.9, bits=4)
+        ora.warmup_step(st_w, g)
+        assert np.array_equal(out["scales"], steps)
+        assert not err.any()
+        for name in ("x", "m", "v"):
+            assert _same_bits(getattr(st_l, name), getattr(st_w, name)), (step, name)
 
 
 PINS = {name[4:]: fn for name, fn in sorted(globals().items())

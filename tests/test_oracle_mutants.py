@@ -50,6 +50,11 @@ MUTANTS = [
      "c[i] = ora_grad(grads, dtype, (int64_t)w * n + i) + comp;",
      "c[i] = ora_grad(grads, dtype, (int64_t)w * n + i);", 0),
     ("loco_ratio_ignored", "float comp = ratio * et[i];", "float comp = et[i];", 0),
+    ("loco_momentum_b2", "float m_old = b1 * m[i];", "float m_old = b2 * m[i];", 1),
+    ("loco_variance_b1", "float v_old = b2 * v[i];", "float v_old = b1 * v[i];", 1),
+    ("loco_dequant_first_chunk_scale",
+     "float deq = (float)q[(int64_t)w * n + i] * scales[(int64_t)w * nchunks + i / C];",
+     "float deq = (float)q[(int64_t)w * n + i] * scales[(int64_t)w * nchunks];", 0),
     ("loco_8bit_codes_shifted", "for (int64_t i = 0; i < n; ++i) cw[i] = (uint8_t)qw[i];",
      "for (int64_t i = 0; i < n; ++i) cw[i] = (uint8_t)(qw[i] + 1);", 0),
     ("loco_levels_off_by_one", "const int levels = (1 << (bits - 1)) - 1;",
