@@ -21,6 +21,8 @@ What pins what:
                     torch.optim.SGD on g / (sqrt(v) + eps), with the weight decay applied
                     to the parameters before the step (decoupled, as AdamW does)
   w1_server         with one worker the server stage reproduces the worker's message
+  server_sum_order  workers added in ascending order (a case where the order rounds
+                    differently)
   mask              masked momentum is exactly zero; unmasked values match the unmasked
                     run; errors are not masked
   warmup_adamw      the warm-up step is AdamW on the mean gradient (torch.optim.AdamW),
@@ -531,6 +533,25 @@ def pin_loco_ratio_zero(ora):
         assert np.array_equal(e, errs[0])
     amax = np.abs(g).reshape(W, -1, C).max(2)
     np.testing.assert_allclose(outs[0]["scales"], amax / 7, rtol=1e-7)
+
+
+def pin_server_sum_order(ora):
+    """The server adds the W decompressed workers in ascending worker order, then divides
+    by W. Three workers with b1 = 0 (so z = g) and constant chunks of 1, 2^-24, 2^-24:
+    their scales are exactly those values; ascending, 1 + 2^-24 rounds back to 1 (a tie,
+    to even) twice, so the average is rn(1/3); in the other order 2^-24 + 2^-24 = 2^-23
+    survives and the average would be rn((1 + 2^-23)/3), a different float32."""
+    n, W, C = 256, 3, 256
+    vals = [1.0, 2.0 ** -24, 2.0 ** -24]
+    g = np.stack([np.full(n, v, np.float32) for v in vals])
+    st = O.OracleState(n, W, C, x=np.zeros(n), m=np.zeros(n), v=np.ones(n), b1=0.0, lr=1e-4)
+    out = ora.compressed_step(st, g)
+    assert np.array_equal(out["wscale"][:, 0], _f32(vals))
+    third = np.float32(np.float32(1.0) / np.float32(3.0))
+    other = np.float32(np.float32(1.0 + 2.0 ** -23) / np.float32(3.0))
+    assert third != other
+    assert np.all(out["y"] == third)
+    assert np.all(st.m == third)                      # constant chunk: T = |y|, all signs +
 
 
 def pin_loco_adam_is_the_warmup_step(ora):

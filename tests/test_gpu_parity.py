@@ -164,6 +164,27 @@ def test_edge_cases(ora, case, C):
         assert np.all(snap["wbits"] == 0xFFFFFFFF) and np.all(snap["wscale"] == 0)
 
 
+@pytest.mark.parametrize("W", [3, 11])
+def test_server_sum_order(ora, W):
+    """Workers added in ascending order on the GPU too, where the order decides the
+    rounding: b1 = 0 (z = g), worker 0's chunk all 1, the others all 2^-24 -- ascending,
+    each 2^-24 rounds away against 1 (through the average table, and for W > 8 the
+    workers after the eighth in order)."""
+    n = W * 256
+    C = 256
+    g = np.full((W, n), 2.0 ** -24, np.float32)
+    g[0] = 1.0
+    st = O.OracleState(n, W, C, x=np.zeros(n), m=np.zeros(n), v=np.ones(n), b1=0.0, lr=1e-4)
+    gpu = CudaPath(st)
+    out = ora.compressed_step(st, g)
+    gpu.compressed_step(g)
+    snap = gpu.snapshot()
+    assert np.array_equal(snap["y"], out["y"])
+    assert np.array_equal(snap["sscale"], out["sscale"])
+    assert np.array_equal(snap["m"], st.m)
+    assert np.array_equal(snap["x"], st.x)
+
+
 def test_deterministic(ora):
     rng = np.random.default_rng(9)
     W, n = 8, 8 * 256 * 500
