@@ -22,7 +22,7 @@ What pins what:
                     to the parameters before the step (decoupled, as AdamW does)
   w1_server         with one worker the server stage reproduces the worker's message
   server_sum_order  workers added in ascending order (a case where the order rounds
-                    differently)
+  mean_orders       differently); the same for the warm-up's and LoCo's means
   mask              masked momentum is exactly zero; unmasked values match the unmasked
                     run; errors are not masked
   warmup_adamw      the warm-up step is AdamW on the mean gradient (torch.optim.AdamW),
@@ -552,6 +552,32 @@ def pin_server_sum_order(ora):
     assert third != other
     assert np.all(out["y"] == third)
     assert np.all(st.m == third)                      # constant chunk: T = |y|, all signs +
+
+
+def pin_mean_orders(ora):
+    """The warm-up's gradient mean and LoCo's dequantized mean add the workers in
+    ascending order too (cases where the order decides the rounding; b1 = 0, so m is the
+    mean itself). Warm-up: 1, 2^-24, 2^-24 as in the server's case. LoCo: worker 0's
+    chunk is all 7 (scale 1, level 7), workers 1 and 2 have level 1 at scale 2^-22 (one
+    element at level 7 sets that scale); ascending, 7 + 2^-22 is a tie that rounds back
+    to 7 twice; in the other order 2^-22 + 2^-22 = 2^-21 would survive."""
+    n, W = 256, 3
+    st = O.OracleState(n, W, n, x=np.zeros(n), m=np.zeros(n), v=np.zeros(n), b1=0.0, lr=1e-4)
+    g = np.stack([np.full(n, v, np.float32) for v in (1.0, 2.0 ** -24, 2.0 ** -24)])
+    ora.warmup_step(st, g)
+    third = np.float32(np.float32(1.0) / np.float32(3.0))
+    assert np.all(st.m == third)
+    g = np.full((W, n), 2.0 ** -22, np.float32)
+    g[0] = 7.0
+    g[1:, 0] = 7.0 * 2.0 ** -22
+    st = O.OracleState(n, W, n, x=np.zeros(n), m=np.zeros(n), v=np.zeros(n), b1=0.0, lr=1e-4)
+    err = np.zeros((W, n), np.float32)
+    out = ora.loco_step(st, g, err, beta=0.0, bits=4)
+    assert np.array_equal(out["scales"][:, 0], _f32([1.0, 2.0 ** -22, 2.0 ** -22]))
+    want = np.float32(np.float32(7.0) / np.float32(3.0))
+    other = np.float32(np.float32(7.0 + 2.0 ** -21) / np.float32(3.0))
+    assert want != other
+    assert np.all(st.m[1:] == want)
 
 
 def pin_loco_adam_is_the_warmup_step(ora):

@@ -185,6 +185,35 @@ def test_server_sum_order(ora, W):
     assert np.array_equal(snap["x"], st.x)
 
 
+def test_warmup_and_loco_mean_orders(ora):
+    """The warm-up and LoCo means add workers in ascending order on the GPU too (the
+    cases where the order decides the rounding, b1 = 0 so m is the mean)."""
+    from gpu_util import to_device_grads
+    n, W = 3 * 256, 3
+    g = np.stack([np.full(n, v, np.float32) for v in (1.0, 2.0 ** -24, 2.0 ** -24)])
+    st = O.OracleState(n, W, n // W, x=np.zeros(n), m=np.zeros(n), v=np.zeros(n), b1=0.0, lr=1e-4)
+    gpu = CudaPath(st)
+    ora.warmup_step(st, g)
+    gpu.warmup_step(g)
+    torch.cuda.synchronize()
+    assert np.array_equal(gpu.m.cpu().numpy(), st.m)
+    assert np.array_equal(gpu.x.cpu().numpy(), st.x)
+
+    g = np.full((W, n), 2.0 ** -22, np.float32)
+    g[0] = 7.0
+    g[1:, ::256] = 7.0 * 2.0 ** -22                  # sets the scale of every chunk
+    st = O.OracleState(n, W, 256, x=np.zeros(n), m=np.zeros(n), v=np.zeros(n), b1=0.0, lr=1e-4)
+    gpu = CudaPath(st)
+    err = np.zeros((W, n), np.float32)
+    err_d = torch.zeros(W, n, dtype=torch.float32, device="cuda")
+    lws = torch.zeros(gpu.ctx.loco_workspace_bytes(4), dtype=torch.uint8, device="cuda")
+    ora.loco_step(st, g, err, beta=0.0, bits=4)
+    gpu.ctx.loco_step(to_device_grads(g, "cuda"), gpu.x, gpu.m, gpu.v, err_d, lws, 0.0, 4)
+    torch.cuda.synchronize()
+    assert np.array_equal(gpu.m.cpu().numpy(), st.m)
+    assert np.array_equal(gpu.x.cpu().numpy(), st.x)
+
+
 def test_deterministic(ora):
     rng = np.random.default_rng(9)
     W, n = 8, 8 * 256 * 500

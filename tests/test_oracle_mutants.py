@@ -24,6 +24,12 @@ MUTANTS = [
      "return (float)sqrt(sum / (double)(C + 1));", 0),
     ("scale_no_sqrt", "return (float)sqrt(sum / (double)C);", "return (float)(sum / (double)C);", 0),
     ("server_sum_not_mean", "float avg = acc / (float)W;", "float avg = acc;", 0),
+    ("warmup_mean_descending",
+     "for (int32_t w = 0; w < W; ++w) acc = acc + ora_grad(grads, dtype, (int64_t)w * n + i);",
+     "for (int32_t w = W - 1; w >= 0; --w) acc = acc + ora_grad(grads, dtype, (int64_t)w * n + i);", 0),
+    ("loco_mean_descending",
+     "for (int32_t w = 0; w < W; ++w) {\n            float deq",
+     "for (int32_t w = W - 1; w >= 0; --w) {\n            float deq", 0),
     ("server_sum_descending", "for (int32_t w = 0; w < W; ++w) {\n            float sent;",
      "for (int32_t w = W - 1; w >= 0; --w) {\n            float sent;", 0),
     ("drop_server_error", "y[i] = avg + server_err[i];", "y[i] = avg;", 0),
