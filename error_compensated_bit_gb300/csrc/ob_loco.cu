@@ -197,7 +197,8 @@ constexpr int kLocoOnePassU = 2;     // groups in flight per sweep (both sweeps 
 template <typename G, int BITS>
 __global__ void __launch_bounds__(kBlock) k_loco_fused(LocoArgs a)
 {
-    constexpr int U = kLocoOnePassU;
+    constexpr int U = kLocoOnePassU;      // second sweep (from the L2)
+    constexpr int UA = kLocoU;            // first sweep (from DRAM): more groups in flight
     const int lane = threadIdx.x & 31;
     const float L = (float)((1 << (BITS - 1)) - 1);
     int64_t s0, s1;
@@ -206,11 +207,11 @@ __global__ void __launch_bounds__(kBlock) k_loco_fused(LocoArgs a)
     for (int64_t slot = s0; slot < s1; ++slot) {
         const int64_t t0 = slot * CG;
         float run = 0.0f;
-        for (int64_t tb = 0; tb < CG; tb += U) {
-            GradRaw<G> gr[U];
-            float ev[U][8];
+        for (int64_t tb = 0; tb < CG; tb += UA) {
+            GradRaw<G> gr[UA];
+            float ev[UA][8];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < UA; ++u) {
                 if (tb + u < CG) {
                     const int64_t e0 = (t0 + tb + u) * 256 + lane * 8;
                     gr[u] = GradRaw<G>::load_l2(a.g, e0);
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kBlock) k_loco_fused(LocoArgs a)
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < UA; ++u) {
                 if (tb + u < CG) {
                     float gv[8];
                     gr[u].widen(gv);
