@@ -107,3 +107,67 @@ class OneBitAdam:
         self.ctx.set_step(int(sd["step"]))
         self.freeze_step = int(sd.get("freeze_step", self.freeze_step))
         self.reset_errors()
+
+
+class LocoAdam:
+    """Adam on LoCo-compressed gradients over one flat float32 buffer and W simulated
+    workers ("LoCo: Low-Bit Communication Adaptor for Large-scale Model Training",
+    "Method"): every step each worker compensates its gradient with ``ratio`` times the
+    moving average of its past compression errors (weight ``beta``), quantizes it per
+    chunk to ``bits``-bit codes with an absmax scale, and the mean of the dequantized
+    gradients drives a plain Adam step.
+
+    The pages say nothing about checkpoints for LoCo; the moving average is part of the
+    compressor's state, so it is saved and restored with the parameters here.
+    """
+
+    def __init__(self, n, W, chunk=None, lr=1e-4, betas=(0.9, 0.999), eps=1e-8,
+                 weight_decay=0.0, bits=4, beta=0.9, ratio=1.0, x=None, device="cuda"):
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        with torch.cuda.device(self.device):
+            self.ctx = ob.Context(n, W, chunk or n // W, betas[0], betas[1], eps, lr)
+            self.ctx.set_options(weight_decay, False)
+            self.ctx.set_loco_ratio(ratio)
+            self.n, self.W, self.chunk = n, W, chunk or n // W
+            self.bits, self.beta, self.ratio = bits, beta, ratio
+            f32 = dict(dtype=torch.float32, device=self.device)
+            self.x = torch.zeros(n, **f32) if x is None else x.to(**f32).contiguous().clone()
+            self.m = torch.zeros(n, **f32)
+            self.v = torch.zeros(n, **f32)
+            self.err = torch.zeros(W, n, **f32)
+            self.ws = torch.zeros(self.ctx.loco_workspace_bytes(bits), dtype=torch.uint8,
+                                  device=self.device)
+
+    @property
+    def step_count(self):
+        return self.ctx.get_step()
+
+    def set_lr(self, lr):
+        self.ctx.set_lr(lr)
+
+    def step(self, grads):
+        """One optimizer step with the [W, n] gradients of the W workers."""
+        with torch.cuda.device(self.device):
+            self.ctx.loco_step(grads, self.x, self.m, self.v, self.err, self.ws, self.beta, self.bits)
+
+    def messages(self):
+        """This step's low-bit messages viewing the workspace: codes [W, n*bits/8] uint8
+        and scales [W, nchunks] float32."""
+        code_bytes = self.W * self.n * self.bits // 8
+        off = (code_bytes + 255) // 256 * 256
+        nch = self.n // self.chunk
+        return (self.ws[:code_bytes].view(self.W, -1),
+                self.ws[off:off + self.W * nch * 4].view(torch.float32).view(self.W, -1))
+
+    def state_dict(self):
+        return {"x": self.x.clone(), "m": self.m.clone(), "v": self.v.clone(),
+                "err": self.err.clone(), "step": self.step_count}
+
+    def load_state_dict(self, sd):
+        self.x.copy_(sd["x"])
+        self.m.copy_(sd["m"])
+        self.v.copy_(sd["v"])
+        self.err.copy_(sd["err"])
+        self.ctx.set_step(int(sd["step"]))

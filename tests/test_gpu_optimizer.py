@@ -73,3 +73,36 @@ def test_checkpoint_resets_errors_and_drops_mask(ora):
     assert_close("x after load", b.x.cpu().numpy(), st.x)
     assert_close("m after load", b.m.cpu().numpy(), st.m)
     assert torch.all(b.m[mask == 0] == 0)
+
+
+def test_loco_adam_matches_oracle_and_resumes(ora):
+    """LocoAdam: 8-bit codes, ratio 1/2, several steps equal to the oracle's LoCo step;
+    a saved state loaded into a fresh object continues identically."""
+    from error_compensated_bit_gb300.optimizer import LocoAdam
+    rng = np.random.default_rng(71)
+    W, n = 3, 3 * 256 * 64
+    C = 256 * 4
+    x0 = rng.standard_normal(n).astype(np.float32) * 0.02
+    opt = LocoAdam(n, W, chunk=C, lr=1e-3, bits=8, beta=0.8, ratio=0.5, x=torch.from_numpy(x0).cuda())
+    st = O.OracleState(n, W, C, x=x0, m=np.zeros(n), v=np.zeros(n), lr=1e-3)
+    err = np.zeros((W, n), np.float32)
+    gs = [_grads(rng, W, n) for _ in range(5)]
+    for t in range(3):
+        opt.step(gs[t])
+        out = ora.loco_step(st, gs[t].cpu().numpy(), err, beta=0.8, bits=8, ratio=0.5)
+        torch.cuda.synchronize()
+        codes, scales = opt.messages()
+        assert np.array_equal(codes.cpu().numpy(), out["codes"])
+        assert np.array_equal(scales.cpu().numpy(), out["scales"])
+        assert np.array_equal(opt.err.cpu().numpy(), err)
+        assert np.array_equal(opt.x.cpu().numpy(), st.x)
+    sd = opt.state_dict()
+    resumed = LocoAdam(n, W, chunk=C, lr=1e-3, bits=8, beta=0.8, ratio=0.5)
+    resumed.load_state_dict(sd)
+    assert resumed.step_count == 3
+    for t in range(3, 5):
+        opt.step(gs[t])
+        resumed.step(gs[t])
+    torch.cuda.synchronize()
+    for name in ("x", "m", "v", "err"):
+        assert torch.equal(getattr(opt, name), getattr(resumed, name)), name
