@@ -53,17 +53,12 @@ __device__ __forceinline__ uint64_t transpose8x8(uint64_t x)
 // a = (sum over w ascending of +-S_wk)/W;  e_s = yprev - T_prev*sign(yprev);  y = a + e_s;
 // bit = (y >= 0); ybuf = y; chunk sums of y^2 -> T_next.
 // Memory per element: W/8 (worker bits) + 4 + 4 (y) + 1/8 (server bits).
-// This lane's sign bytes of group gi from every worker row: byte (lane & 3) of word
-// (lane >> 2) of the group's eight words in row w becomes byte w of the result (rows W
-// and above give zero bytes). Two rounds of byte permutes gather four rows into one word.
-template <int W>
-__device__ __forceinline__ uint64_t gather_sign_bytes(const uint32_t* wbits, int64_t words_per_row, int64_t gi,
-                                                      int lane)
+// This lane's sign bytes from the words holding its elements' sign bits in each worker
+// row (word lane >> 2 of the group's eight; zero for rows W and above): byte (lane & 3)
+// of row w's word becomes byte w of the result. Two rounds of byte permutes gather four
+// rows into one word.
+__device__ __forceinline__ uint64_t pack_sign_bytes(const uint32_t (&wv)[8], int lane)
 {
-    const uint32_t* p = wbits + gi * 8 + (lane >> 2);
-    uint32_t wv[8];
-#pragma unroll
-    for (int w = 0; w < 8; ++w) wv[w] = w < W ? __ldcs(p + (int64_t)w * words_per_row) : 0u;
     const uint32_t b = (uint32_t)lane & 3u;
     const uint32_t pick = b | ((b + 4u) << 4);        // byte b of the first and of the second word
     const uint32_t lo = __byte_perm(__byte_perm(wv[0], wv[1], pick), __byte_perm(wv[2], wv[3], pick), 0x5410);
@@ -71,9 +66,12 @@ __device__ __forceinline__ uint64_t gather_sign_bytes(const uint32_t* wbits, int
     return ((uint64_t)hi << 32) | lo;
 }
 
-// Used for W <= 8: one group's loads per warp in flight, 64 registers (four blocks per SM).
-// Keeping several groups in flight through shared memory (k_server_staged) measured slower
-// here, where the pass is close to bound by instruction issue; it pays for W > 8.
+// Used for W <= 8: one group's y per warp in flight, 64 registers (four blocks per SM). The
+// worker sign words come in one coalesced 128-byte load per row for four groups at a time
+// (lane l holds word l), and each group takes its words from the holding lanes by
+// shuffles: a quarter of the load requests of a 32-byte load per row and group, 5-6%
+// faster. Keeping several groups in flight through shared memory (cp.async copies as in
+// k_server_staged, or bulk copies) measured slower here; it pays for W > 8.
 template <int W>
 __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
 {
@@ -88,12 +86,14 @@ __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
     pdl_wait();             // the worker pass has finished
     pdl_allow_next();
 
+    // group and chunk indices fit 32 bits (W * n / 256 < 2^32 is checked at init)
+    const uint32_t CG = (uint32_t)pt.CG;
     for (int64_t q = warp; q < pt.P; q += nwarps) {
-        const int64_t g0 = range_begin(pt, q);
-        const int64_t g1 = range_begin(pt, q + 1);
-        int64_t k = g0 / pt.CG;
-        const int64_t kfirst = k;
-        int64_t kend = (k + 1) * pt.CG;
+        const uint32_t g0 = (uint32_t)range_begin(pt, q);
+        const uint32_t g1 = (uint32_t)range_begin(pt, q + 1);
+        uint32_t k = g0 / CG;
+        const uint32_t kfirst = k;
+        uint32_t kend = (k + 1) * CG;
 
         float sw[W];
 #pragma unroll
@@ -101,20 +101,32 @@ __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
         float tp = __ldg(a.t_prev + k);
         build_average_table<W>(tab, sw, lane);
         Sum2 acc[1] = {{0.0f, 0.0f}};
+        uint32_t blk[8];    // row w: word `lane` of the 32 words of groups 4b .. 4b + 3
 
-        for (int64_t gi = g0; gi < g1; ++gi) {
+        for (uint32_t gi = g0; gi < g1; ++gi) {
             if (gi == kend) {
                 flush_chunk<1, kFlushInline>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
                 ++k;
-                kend += pt.CG;
+                kend += CG;
 #pragma unroll
                 for (int w = 0; w < W; ++w) sw[w] = __ldg(a.s_next + (int64_t)w * pt.nchunks + k);
                 tp = __ldg(a.t_prev + k);
                 build_average_table<W>(tab, sw, lane);
             }
-            const uint64_t raw = gather_sign_bytes<W>(a.wbits, words_per_row, gi, lane);
+            const int jg = (int)(gi & 3u);
+            if (jg == 0 || gi == g0) {
+                // one coalesced 128-byte load per row covers this group and the next three
+                const int64_t wb = (int64_t)(gi & ~3u) * 8 + lane;
+                const bool in = wb < words_per_row;
+#pragma unroll
+                for (int w = 0; w < W; ++w) blk[w] = in ? __ldcs(a.wbits + (int64_t)w * words_per_row + wb) : 0u;
+            }
+            uint32_t wv[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) wv[w] = w < W ? __shfl_sync(kFull, blk[w], jg * 8 + (lane >> 2)) : 0u;
+            const uint64_t raw = pack_sign_bytes(wv, lane);
             float yv[8];
-            ld8_stream(a.ybuf + gi * 256 + lane * 8, yv);
+            ld8_stream(a.ybuf + (int64_t)gi * 256 + lane * 8, yv);
             const uint64_t pat = transpose8x8(raw);   // byte j: element j's signs, bit w = worker w
             uint32_t byte = 0;
 #pragma unroll
@@ -126,9 +138,9 @@ __global__ void __launch_bounds__(kBlock, 4) k_server(ServerArgs a)
                 byte |= (y >= 0.0f ? 1u : 0u) << j;
                 sum2_add_sq(acc[0], y);
             }
-            st8_stream(a.ybuf + gi * 256 + lane * 8, yv);
+            st8_stream(a.ybuf + (int64_t)gi * 256 + lane * 8, yv);
             const uint32_t word = quad_word(byte, lane);
-            if ((lane & 3) == 0) __stcs(a.sbits + gi * 8 + (lane >> 2), word);
+            if ((lane & 3) == 0) __stcs(a.sbits + (int64_t)gi * 8 + (lane >> 2), word);
         }
         flush_chunk<1, kFlushInline>(pt, q, 1, 0, k, kfirst, g0, g1, acc, a.part, a.cnt, a.t_next, a.C, a.ybuf, a.n, lane);
     }
@@ -280,16 +292,22 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
 
     for (int64_t gb = warp * a.NG / nwarps; gb < g_end; gb += U) {
         float vv[U][8], xv[U][8];
-        uint32_t sb[U], mb[U];
         float T[U];
+        uint32_t sb[U];
+        // masked: the U groups' server and mask words in one coalesced load per bit row
+        // (lane l holds word l of the 8U words from group gb on; measured faster there,
+        // and slower than one word per lane and group without a mask)
+        const int64_t wb = gb * 8 + lane;
+        const bool win = masked && lane < 8 * U && wb < g_end * 8;
+        const uint32_t swd = win ? __ldcs(a.sbits + wb) : 0u;
+        const uint32_t mwd = win ? __ldcs(a.maskbits + wb) : 0u;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t gi = gb + u;
             if (gi < g_end) {
                 const int64_t e0 = gi * 256 + lane * 8;
                 T[u] = __ldg(a.t_next + fast_div((uint32_t)gi, a.cg_div));
-                sb[u] = lane_byte(a.sbits, gi, lane);
-                mb[u] = masked ? lane_byte(a.maskbits, gi, lane) : 0xffu;
+                if (!masked) sb[u] = lane_byte(a.sbits, gi, lane);
                 ld8_stream(a.v + e0, vv[u]);
                 ld8_stream(a.x + e0, xv[u]);
             }
@@ -297,19 +315,26 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t gi = gb + u;
+            uint32_t sbu = sb[u], mbu = 0xffu;
+            if (masked) {
+                // this lane's 8 bits of group gi: byte (lane & 3) of the group's word lane >> 2
+                const int src = u * 8 + (lane >> 2);
+                sbu = (__shfl_sync(kFull, swd, src) >> (8 * (lane & 3))) & 0xffu;
+                mbu = (__shfl_sync(kFull, mwd, src) >> (8 * (lane & 3))) & 0xffu;
+            }
             if (gi < g_end) {
                 const int64_t e0 = gi * 256 + lane * 8;
                 float mv[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float st = signed_scale(T[u], (sb[u] >> j) & 1u);
+                    const float st = signed_scale(T[u], (sbu >> j) & 1u);
                     const float denom = __fadd_rn(__fsqrt_rn(vv[u][j]), a.eps);
                     float mi = st, uu;
                     if (masked) {
                         // a masked element has mi = st*0 = +-0 and mi/denom = mi (denom > 0);
                         // the quotient is formed from st and then selected, so the division
                         // never sees the zero numerators that send it down its slow path
-                        const bool on = ((mb[u] >> j) & 1u) != 0u;
+                        const bool on = ((mbu >> j) & 1u) != 0u;
                         mi = __fmul_rn(st, on ? 1.0f : 0.0f);
                         const float q = __fdiv_rn(st, denom);
                         uu = on ? q : mi;
