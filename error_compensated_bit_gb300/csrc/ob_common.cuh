@@ -272,6 +272,15 @@ __device__ __forceinline__ Sum2 warp_reduce_rows(const Sum2 (&v)[R], int lane, i
     return x[0];
 }
 
+// After warp_reduce_rows<R>: whether this lane is the one that stores its row's total
+// (the lowest lane of each group of lanes left holding the same row).
+template <int R>
+__device__ __forceinline__ bool row_holder(int lane, int row)
+{
+    constexpr int P2 = R <= 1 ? 1 : (R <= 2 ? 2 : (R <= 4 ? 4 : (R <= 8 ? 8 : 16)));
+    return (lane & (32 / P2 - 1)) == 0 && row < R;
+}
+
 // sqrt(sum / C) rounded to float32, from a sum of squares held as a float pair, in
 // double-float arithmetic (T. J. Dekker, "A floating-point technique for extending the
 // available precision", 1971): the quotient's exact remainder by FMA gives its trailing
@@ -293,6 +302,20 @@ __device__ __forceinline__ bool rms_from_pair(const Sum2& t, float Cf, float& ou
     const float sl = __fdiv_rn(d, __fadd_rn(sh, sh));
     out = __fadd_rn(sh, sl);
     return true;
+}
+
+// A chunk's scale from its double sum of squares: the sum split into a float pair (its
+// float rounding and the float rounding of the remainder, which is exact in double) and
+// the root taken by rms_from_pair in float arithmetic -- double division and square root
+// are slow on this part, and this runs on the launch's critical path (the last
+// contributor of each chunk). Sums outside rms_from_pair's range take the double root.
+__device__ __forceinline__ float rms_from_double(double sum, int64_t C)
+{
+    const float hi = (float)sum;
+    const float lo = (float)(sum - (double)hi);
+    float sc;
+    if (C <= (1 << 24) && rms_from_pair(Sum2{hi, lo}, (float)C, sc)) return sc;
+    return (float)sqrt(sum / (double)C);
 }
 
 // Butterfly sum: every lane ends with the same, order-fixed value.
@@ -377,7 +400,7 @@ __device__ __forceinline__ void combine_chunk(const Part& pt, int wpr, int64_t k
         for (int r = 0; r < R; ++r) {
             double sum = warp_sum(acc_r[r]);
             if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
-            if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(sum / (double)C);
+            if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = rms_from_double(sum, C);
         }
     } else {
         // several warps per range: lane l owns the (row, warp) pairs l, l+32, ... and adds
@@ -419,7 +442,7 @@ __device__ __forceinline__ void combine_chunk(const Part& pt, int wpr, int64_t k
                 if (row_of[i] == r) v += acc_p[i];
             double sum = warp_sum(v);
             if (!sumsq_trusted(sum, C)) sum = chunk_sumsq_exact(rows + (int64_t)r * row_stride + k * C, C, lane);
-            if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = (float)sqrt(sum / (double)C);
+            if (lane == 0) scale_out[(int64_t)r * pt.nchunks + k] = rms_from_double(sum, C);
         }
     }
     if (lane == 0) cnt[k] = 0u;
@@ -436,8 +459,7 @@ template <int R>
 __device__ __forceinline__ void sole_scales(Sum2 t, int row, const Part& pt, int64_t k, float* scale_out,
                                             int64_t C, const float* rows, int64_t row_stride, int lane)
 {
-    constexpr int P2 = R <= 1 ? 1 : (R <= 2 ? 2 : (R <= 4 ? 4 : (R <= 8 ? 8 : 16)));
-    const bool holder = (lane & (32 / P2 - 1)) == 0 && row < R;   // one lane per row
+    const bool holder = row_holder<R>(lane, row);   // one lane per row
     float sc = 0.0f;
     const bool ok = C <= (1 << 24) && rms_from_pair(t, (float)C, sc);
     unsigned bad = __ballot_sync(kFull, holder && !ok);

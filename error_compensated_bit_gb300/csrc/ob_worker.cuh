@@ -102,10 +102,23 @@ __device__ __forceinline__ void flush_chunk_block(const Part& pt, int64_t q, int
                                                   int64_t row_stride, int lane)
 {
     const int j = (int)(k - kfirst);
+    if constexpr (W <= 4) {
+        // few rows: the warp's row totals as float pairs spread over the lanes, each row's
+        // holder storing its total as one double. Double operations are slow on this part
+        // (per-row double butterflies kept its double pipe busy for about a quarter of a
+        // small launch's worker time), and up to four rows reduce-scatter in registers.
+        int row;
+        const Sum2 t = warp_reduce_rows<W>(acc, lane, row);
+        if (row_holder<W>(lane, row)) bpart[(j * kMaxWarps + wib) * W + row] = (double)t.s + (double)t.e;
+    } else {
+#pragma unroll
+        for (int r = 0; r < W; ++r) {
+            const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
+            if (lane == 0) bpart[(j * kMaxWarps + wib) * W + r] = d;
+        }
+    }
 #pragma unroll
     for (int r = 0; r < W; ++r) {
-        const double d = warp_sum((double)acc[r].s + (double)acc[r].e);
-        if (lane == 0) bpart[(j * kMaxWarps + wib) * W + r] = d;
         acc[r].s = 0.0f;
         acc[r].e = 0.0f;
     }
