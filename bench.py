@@ -277,12 +277,19 @@ KERNEL_OF_PHASE = {"compressed": "worker", "warmup": "warmup", "loco": "loco_qua
 GRAD_BUFFERS = 3        # per-step gradient draws, cycled through in every timed loop
 
 
-def dominant_kernel_bytes(phase, n, W, s_g):
+LOCO_ONE_PASS_MAX_CHUNK = 4096    # LoCo chunks up to this long: absmax and quantize in one pass
+
+
+def dominant_kernel_bytes(phase, n, W, s_g, chunk=None):
     """Algorithmic bytes of one launch of the phase's dominant kernel."""
     if phase == "compressed":
         return n * worker_bytes_per_elem(W, s_g)
     if phase == "warmup":
         return n * (W * s_g + 24.0)
+    if chunk is not None and chunk > LOCO_ONE_PASS_MAX_CHUNK:
+        # LoCo, long chunks: quantize every row and take the Adam step in one pass
+        # (g, e read and e written per row; x, m, v read and written; codes kept in registers)
+        return n * (W * (s_g + 8.0) + 24.0)
     return n * W * (s_g + 8.5)                     # LoCo quantize: g, e read; e, codes written
 
 
@@ -416,7 +423,7 @@ class Run:
         ctx.profile(False)
         del scratch
         dom = KERNEL_OF_PHASE[self.phase]
-        k_bytes = dominant_kernel_bytes(self.phase, self.wl.n, self.wl.W, self.wl.grad_bytes)
+        k_bytes = dominant_kernel_bytes(self.phase, self.wl.n, self.wl.W, self.wl.grad_bytes, self.wl.C)
         k_avg_us = per_kernel[dom]["avg_us"] if dom in per_kernel else None
         return {"ms_total": ms_total, "steps": steps, "b_step": b_step, "flush": flush,
                 "kernel_events_pass": "separate" if separate else "same",

@@ -42,6 +42,7 @@ struct ob_ctx {
     int W = 0;
     float b1 = 0, b2 = 0, eps = 0, lr = 0, wd = 0;
     float loco_ratio = 1.0f;    // LoCo: share of the averaged error compensated into g
+    bool loco_codes = false;    // LoCo, long chunks: also store the codes
     int bias_correction = 0;
     int64_t step = 0;
     int device = -1;
@@ -52,9 +53,9 @@ struct ob_ctx {
     Part pts{};                 // server partition
     int grid_s = 0;
     int grid_u = 0;             // update kernel: one resident wave
-    int loco_occ_a[3] = {};     // resident blocks per SM of the LoCo absmax / quantize
-    int loco_occ_q[3][2] = {};  // passes (per gradient type and code width; 0 = not asked)
-    int loco_occ_f[3][2] = {};  // the same for the one-pass short-chunk kernel
+    int loco_occ_a[3] = {};     // resident blocks per SM of the LoCo absmax pass (per gradient type)
+    int loco_occ_f[3][2] = {};  // the same for the one-pass short-chunk kernel (and code width)
+    int loco_occ_qs[3][2] = {}; // and for the long-chunk quantize + server kernel (0 = not asked)
     Layout lay{};
     bool has_mask = false;
     int64_t launches = 0;
@@ -335,6 +336,13 @@ int ob_set_loco_ratio(ob_ctx* c, float ratio)
     return OB_OK;
 }
 
+int ob_set_loco_codes(ob_ctx* c, int keep)
+{
+    if (!c || (keep != 0 && keep != 1)) return OB_EINVAL;
+    c->loco_codes = keep != 0;
+    return OB_OK;
+}
+
 int ob_set_step(ob_ctx* c, int64_t step)
 {
     if (!c || step < 0) return OB_EINVAL;
@@ -584,6 +592,7 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     a.W = c->W;
     a.bits = bits;
     a.ratio = c->loco_ratio;
+    a.keep_codes = c->loco_codes ? 1 : 0;
     a.beta = beta;
     a.keep = 1.0f - beta;
     a.b1 = c->b1;
@@ -606,15 +615,14 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     }
     const cudaError_t e = cudaMemsetAsync(a.amax_bits, 0, (size_t)c->W * c->nchunks * 4, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    // the absmax and quantize passes: one resident wave, each warp a contiguous range;
-    // the server pass: four blocks per SM (its full wave), grid-stride
+    // the absmax pass, then one pass that quantizes every row and takes the server step:
+    // each one resident wave, each warp a contiguous range
     if (!c->loco_occ_a[dtype]) c->loco_occ_a[dtype] = occupancy_loco_absmax(dtype);
-    if (!c->loco_occ_q[dtype][bi]) c->loco_occ_q[dtype][bi] = occupancy_loco_quant(dtype, bits);
+    if (!c->loco_occ_qs[dtype][bi]) c->loco_occ_qs[dtype][bi] = occupancy_loco_qs(dtype, bits);
     const int grid_a = c->sms * (c->loco_occ_a[dtype] > 0 ? c->loco_occ_a[dtype] : 2);
-    const int grid_q = c->sms * (c->loco_occ_q[dtype][bi] > 0 ? c->loco_occ_q[dtype][bi] : 2);
+    const int grid_qs = c->sms * (c->loco_occ_qs[dtype][bi] > 0 ? c->loco_occ_qs[dtype][bi] : 2);
     if (int r = launch(c, OB_K_LOCO_ABSMAX, s, [&] { return launch_loco_absmax(dtype, a, grid_a, s); })) return r;
-    if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_quant(dtype, a, grid_q, s); })) return r;
-    if (int r = launch(c, OB_K_LOCO_SERVER, s, [&] { return launch_loco_server(a, grid, s); })) return r;
+    if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_qs(dtype, a, grid_qs, s); })) return r;
     c->step += 1;
     return OB_OK;
 }

@@ -136,6 +136,7 @@ struct LocoArgs {
     int64_t n, C, nchunks, NG;
     FastDiv ng_div, cg_div;    // division by the groups per row / per chunk
     int W, bits;
+    int keep_codes;        // long chunks: also store the codes (they are otherwise kept in registers)
     float ratio, beta, keep, b1, c1, b2, c2, eps, lr, wd;
 };
 
@@ -155,15 +156,15 @@ cudaError_t launch_warmup(int dtype, const WarmupArgs& a, int grid, cudaStream_t
 cudaError_t launch_mask(const MaskArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_export(const ExportArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_absmax(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_loco_qs(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_loco_fused(int dtype, const LocoArgs& a, int grid, cudaStream_t s);
 
 // Resident blocks per SM of the server kernel for W / of the update kernel; 0 on error.
 int occupancy_server(int W);
 int occupancy_update();
 int occupancy_loco_absmax(int dtype);
-int occupancy_loco_quant(int dtype, int bits);
+int occupancy_loco_qs(int dtype, int bits);
 int occupancy_loco_fused(int dtype, int bits, int64_t C);
 
 // Launch `kernel` with the programmatic stream-serialization attribute (see pdl_wait in

@@ -8,18 +8,19 @@
 // compression, then synchronise), key design item 2 (the proportion of the compensation
 // is tuned: `ratio`, 1 by default) and the abstract (compatible with Adam).
 //
-// Three passes for long chunks. The absmax of c = g + ratio*e~ over a chunk must be known
-// before any element of the chunk can be quantized, and a chunk spans up to n/W
-// elements, so c is formed twice (pass 1 for the absmax, pass 2 to quantize) instead of
-// being stored.
-//   pass 1  amax[w][k] = max |c|                         (atomicMax on float bits: exact)
-//   pass 2  s = amax/L; q = clamp(rint(c/s), -L, L) (0 when s = 0); e = c - q*s;
-//           e~ = beta*e~ + (1-beta)*e; codes <- q
-//   pass 3  gbar = (sum over w of q_w*s_w)/W; Adam on m, v, x
-// Memory per element: pass 1 W*(grad+4), pass 2 W*(grad+8+bits/8), pass 3
-// W*bits/8 + 24. Chunks of up to 4096 elements take passes 1 and 2 in one kernel whose
-// warps own whole chunks (k_loco_fused_small, k_loco_fused), reading the gradients and
-// errors from DRAM once.
+// Passes. The absmax of c = g + ratio*e~ over a chunk must be known before any element of
+// the chunk can be quantized, and a chunk spans up to n/W elements, so for long chunks c
+// is formed twice (once for the absmax, once to quantize) instead of being stored:
+//   absmax     amax[w][k] = max |c|                      (atomicMax on float bits: exact)
+//   quantize   s = amax/L; q = clamp(rint(c/s), -L, L) (0 when s = 0); e = c - q*s;
+//              e~ = beta*e~ + (1-beta)*e
+//   server     gbar = (sum over w of q_w*s_w)/W; Adam on m, v, x
+// Long chunks: the absmax pass (W*(grad+4) bytes per element), then quantize and server
+// in one pass over all W rows of each group (k_loco_qs: W*(grad+8) + 24; the codes stay
+// in registers). Chunks of up to 4096 elements: absmax and quantize in one kernel whose
+// warps own whole chunks (k_loco_fused_small, k_loco_fused: W*(grad+8+bits/8), reading
+// the gradients and errors from DRAM once), then the server pass (k_loco_server:
+// W*bits/8 + 24).
 #include "ob_common.cuh"
 #include "ob_div.cuh"
 
@@ -93,14 +94,13 @@ __global__ void __launch_bounds__(kBlock) k_loco_absmax(LocoArgs a)
 }
 
 // Quantize one lane's 8 elements of a group with scale s (inv = rn(1/s)) and update the
-// moving average of the errors in place; returns the codes packed as stored.
+// moving average of the errors in place; returns the levels.
 template <int BITS>
-__device__ __forceinline__ void quantize8(const float (&gv)[8], float (&ev)[8], float s, float inv,
-                                          float ratio, float beta, float keep, uint32_t& lo, uint32_t& hi)
+__device__ __forceinline__ void quantize8_levels(const float (&gv)[8], float (&ev)[8], float s, float inv,
+                                                 float ratio, float beta, float keep, int (&qv)[8])
 {
     const float L = (float)((1 << (BITS - 1)) - 1);
     constexpr float kTieMargin = (float)(1 << (BITS - 1)) * 0x1p-21f;   // (L + 1) 2^-21
-    int qv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const float c = __fadd_rn(gv[j], __fmul_rn(ratio, ev[j]));
@@ -121,6 +121,13 @@ __device__ __forceinline__ void quantize8(const float (&gv)[8], float (&ev)[8], 
         const float e = __fsub_rn(c, __fmul_rn((float)qi, s));
         ev[j] = __fadd_rn(__fmul_rn(beta, ev[j]), __fmul_rn(keep, e));
     }
+}
+
+// The levels packed as stored: 4 bits two per byte (even element in the low nibble) or
+// one signed byte each, two's complement.
+template <int BITS>
+__device__ __forceinline__ void pack_codes(const int (&qv)[8], uint32_t& lo, uint32_t& hi)
+{
     lo = 0;
     hi = 0;
     if (BITS == 4) {
@@ -135,53 +142,21 @@ __device__ __forceinline__ void quantize8(const float (&gv)[8], float (&ev)[8], 
     }
 }
 
-template <typename G, int BITS>
-__global__ void __launch_bounds__(kBlock) k_loco_quant(LocoArgs a)
+template <int BITS>
+__device__ __forceinline__ void store_codes(uint8_t* out, uint32_t lo, uint32_t hi)
 {
-    constexpr int U = kLocoU;
-    const int lane = threadIdx.x & 31;
-    const float L = (float)((1 << (BITS - 1)) - 1);
-    int64_t t0, t1;
-    warp_items((int64_t)a.W * a.NG, t0, t1);
-    const int64_t CG = a.C / 256;
-    // scale of the slot the warp is in, and its reciprocal; formed again only when the
-    // slot changes (a warp's range crosses one or two slots)
-    int64_t cur = -1;
-    float s = 0.0f, inv = 0.0f;
-    for (int64_t tb = t0; tb < t1; tb += U) {
-        GradRaw<G> gr[U];
-        float ev[U][8];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (tb + u < t1) {
-                const int64_t e0 = (tb + u) * 256 + lane * 8;
-                gr[u] = GradRaw<G>::load(a.g, e0);
-                ld8_stream(a.err + e0, ev[u]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t t = tb + u;
-            if (t < t1) {
-                const int64_t key = fast_div((uint32_t)t, a.cg_div);
-                if (key != cur) {
-                    cur = key;
-                    s = __fdiv_rn(__uint_as_float(__ldcg(a.amax_bits + key)), L);
-                    inv = __frcp_rn(s);
-                }
-                if (lane == 0 && t == key * CG) a.scale[key] = s;
-                float gv[8];
-                gr[u].widen(gv);
-                uint32_t lo, hi;
-                quantize8<BITS>(gv, ev[u], s, inv, a.ratio, a.beta, a.keep, lo, hi);
-                const int64_t e0 = t * 256 + lane * 8;
-                st8_stream(a.err + e0, ev[u]);
-                uint8_t* out = a.codes + e0 * BITS / 8;
-                if (BITS == 4) __stcs(reinterpret_cast<unsigned int*>(out), lo);
-                else __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
-            }
-        }
-    }
+    if (BITS == 4) __stcs(reinterpret_cast<unsigned int*>(out), lo);
+    else __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
+}
+
+// quantize8_levels, then the levels packed as stored.
+template <int BITS>
+__device__ __forceinline__ void quantize8(const float (&gv)[8], float (&ev)[8], float s, float inv,
+                                          float ratio, float beta, float keep, uint32_t& lo, uint32_t& hi)
+{
+    int qv[8];
+    quantize8_levels<BITS>(gv, ev, s, inv, ratio, beta, keep, qv);
+    pack_codes<BITS>(qv, lo, hi);
 }
 
 // Absmax and quantization in one kernel, for chunks short enough that a warp owns whole
@@ -251,9 +226,7 @@ __global__ void __launch_bounds__(kBlock) k_loco_fused(LocoArgs a)
                     quantize8<BITS>(gv, ev[u], s, inv, a.ratio, a.beta, a.keep, lo, hi);
                     const int64_t e0 = (t0 + tb + u) * 256 + lane * 8;
                     st8_stream(a.err + e0, ev[u]);
-                    uint8_t* out = a.codes + e0 * BITS / 8;
-                    if (BITS == 4) __stcs(reinterpret_cast<unsigned int*>(out), lo);
-                    else __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
+                    store_codes<BITS>(a.codes + e0 * BITS / 8, lo, hi);
                 }
             }
         }
@@ -318,9 +291,7 @@ __global__ void __launch_bounds__(kBlock, sizeof(G) == 4 ? 2 : 3) k_loco_fused_s
                 quantize8<BITS>(gv, ev[u], sc, inv, a.ratio, a.beta, a.keep, lo, hi);
                 const int64_t e0 = (tb + u) * 256 + lane * 8;
                 st8_stream(a.err + e0, ev[u]);
-                uint8_t* out = a.codes + e0 * BITS / 8;
-                if (BITS == 4) __stcs(reinterpret_cast<unsigned int*>(out), lo);
-                else __stcs(reinterpret_cast<uint2*>(out), make_uint2(lo, hi));
+                store_codes<BITS>(a.codes + e0 * BITS / 8, lo, hi);
             }
         }
     }
@@ -340,6 +311,23 @@ __device__ __forceinline__ void load_codes(const uint8_t* p, int (&q)[8])
             q[j] = ((int)(r.x << (24 - 8 * j))) >> 24;
             q[j + 4] = ((int)(r.y << (24 - 8 * j))) >> 24;
         }
+    }
+}
+
+// The Adam step on one lane's 8 elements from the sum over workers of the dequantized
+// gradients (gbar = acc/W): m, v, x updated in place.
+__device__ __forceinline__ void loco_adam8(const float (&acc)[8], float fW, float (&mv)[8], float (&vv)[8],
+                                           float (&xv)[8], const LocoArgs& a)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float gbar = div_rn_zero_fast(acc[j], fW);
+        mv[j] = __fadd_rn(__fmul_rn(a.b1, mv[j]), __fmul_rn(a.c1, gbar));
+        vv[j] = __fadd_rn(__fmul_rn(a.b2, vv[j]), __fmul_rn(a.c2, __fmul_rn(gbar, gbar)));
+        const float denom = __fadd_rn(__fsqrt_rn(vv[j]), a.eps);
+        float u = div_rn_zero_fast(mv[j], denom);
+        if (a.wd != 0.0f) u = __fadd_rn(u, __fmul_rn(a.wd, xv[j]));
+        xv[j] = __fsub_rn(xv[j], __fmul_rn(a.lr, u));
     }
 }
 
@@ -367,16 +355,84 @@ __global__ void __launch_bounds__(kBlock) k_loco_server(LocoArgs a)
         ld8_stream(a.m + e0, mv);
         ld8_stream(a.v + e0, vv);
         ld8_stream(a.x + e0, xv);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float gbar = div_rn_zero_fast(acc[j], fW);
-            mv[j] = __fadd_rn(__fmul_rn(a.b1, mv[j]), __fmul_rn(a.c1, gbar));
-            vv[j] = __fadd_rn(__fmul_rn(a.b2, vv[j]), __fmul_rn(a.c2, __fmul_rn(gbar, gbar)));
-            const float denom = __fadd_rn(__fsqrt_rn(vv[j]), a.eps);
-            float u = div_rn_zero_fast(mv[j], denom);
-            if (a.wd != 0.0f) u = __fadd_rn(u, __fmul_rn(a.wd, xv[j]));
-            xv[j] = __fsub_rn(xv[j], __fmul_rn(a.lr, u));
+        loco_adam8(acc, fW, mv, vv, xv, a);
+        st8_stream(a.m + e0, mv);
+        st8_stream(a.v + e0, vv);
+        st8_stream(a.x + e0, xv);
+    }
+}
+
+// Long chunks, after the absmax pass: the quantization of every worker row and the server
+// step in one pass. Each block works one contiguous, balanced range of groups (the grid is
+// one resident wave) and its warps take the range's groups in turn; per group a warp
+// quantizes the W rows in ascending order, with the next row's loads in flight while one
+// row is quantized, adds each dequantized row into the sum in that order, and takes the
+// Adam step on x, m, v. The codes stay in registers (stored only when a.keep_codes is set),
+// so DRAM sees neither their write nor their read-back: W*(grad + 8) + 24 bytes per
+// element instead of W*(grad + 8 + bits/4) + 24 for a quantize pass and a server pass.
+// Scales, codes, errors and the Adam state are those of the separate passes exactly: the
+// same quantize8_levels, the same sums in the same order.
+template <typename G, int BITS>
+__global__ void __launch_bounds__(kBlock, 2) k_loco_qs(LocoArgs a)
+{
+    __shared__ float2 s_sc[kBlock / 32][16];   // per warp: (s, rn(1/s)) of each row in its chunk
+    const int lane = threadIdx.x & 31;
+    float2* sc = s_sc[threadIdx.x >> 5];
+    const float L = (float)((1 << (BITS - 1)) - 1);
+    const int wpb = blockDim.x >> 5;
+    const int64_t g_end = ((int64_t)blockIdx.x + 1) * a.NG / gridDim.x;
+    const int64_t CG = a.C / 256;
+    const float fW = (float)a.W;
+    int64_t cur = -1;
+    for (int64_t gi = (int64_t)blockIdx.x * a.NG / gridDim.x + (threadIdx.x >> 5); gi < g_end; gi += wpb) {
+        const int64_t k = fast_div((uint32_t)gi, a.cg_div);
+        if (k != cur) {
+            // the rows' scales of chunk k, formed once per chunk the warp enters; the warp
+            // holding the chunk's first group stores them
+            cur = k;
+            __syncwarp();
+            if (lane < a.W) {
+                const float s = __fdiv_rn(__uint_as_float(__ldcg(a.amax_bits + (int64_t)lane * a.nchunks + k)), L);
+                sc[lane] = make_float2(s, __frcp_rn(s));
+                if (gi == k * CG) a.scale[(int64_t)lane * a.nchunks + k] = s;
+            }
+            __syncwarp();
         }
+        const int64_t e0 = gi * 256 + lane * 8;
+        float mv[8], vv[8], xv[8], ev[8], acc[8];
+        ld8_stream(a.m + e0, mv);
+        ld8_stream(a.v + e0, vv);
+        ld8_stream(a.x + e0, xv);
+        GradRaw<G> gr = GradRaw<G>::load(a.g, e0);
+        ld8_stream(a.err + e0, ev);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int w = 0; w < a.W; ++w) {
+            const int64_t ew = (int64_t)w * a.n + e0;
+            GradRaw<G> gn = gr;
+            float en[8];
+            if (w + 1 < a.W) {
+                gn = GradRaw<G>::load(a.g, ew + a.n);
+                ld8_stream(a.err + ew + a.n, en);
+            }
+            float gv[8];
+            gr.widen(gv);
+            const float2 si = sc[w];
+            int qv[8];
+            quantize8_levels<BITS>(gv, ev, si.x, si.y, a.ratio, a.beta, a.keep, qv);
+            st8_stream(a.err + ew, ev);
+            if (a.keep_codes) {
+                uint32_t lo, hi;
+                pack_codes<BITS>(qv, lo, hi);
+                store_codes<BITS>(a.codes + ew * BITS / 8, lo, hi);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn((float)qv[j], si.x));
+            gr = gn;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ev[j] = en[j];
+        }
+        loco_adam8(acc, fW, mv, vv, xv, a);
         st8_stream(a.m + e0, mv);
         st8_stream(a.v + e0, vv);
         st8_stream(a.x + e0, xv);
@@ -388,20 +444,6 @@ cudaError_t launch_loco_absmax(int dtype, const LocoArgs& a, int grid, cudaStrea
     if (dtype == 0) k_loco_absmax<float><<<grid, kBlock, 0, s>>>(a);
     else if (dtype == 1) k_loco_absmax<__half><<<grid, kBlock, 0, s>>>(a);
     else k_loco_absmax<__nv_bfloat16><<<grid, kBlock, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_loco_quant(int dtype, const LocoArgs& a, int grid, cudaStream_t s)
-{
-    if (a.bits == 4) {
-        if (dtype == 0) k_loco_quant<float, 4><<<grid, kBlock, 0, s>>>(a);
-        else if (dtype == 1) k_loco_quant<__half, 4><<<grid, kBlock, 0, s>>>(a);
-        else k_loco_quant<__nv_bfloat16, 4><<<grid, kBlock, 0, s>>>(a);
-    } else {
-        if (dtype == 0) k_loco_quant<float, 8><<<grid, kBlock, 0, s>>>(a);
-        else if (dtype == 1) k_loco_quant<__half, 8><<<grid, kBlock, 0, s>>>(a);
-        else k_loco_quant<__nv_bfloat16, 8><<<grid, kBlock, 0, s>>>(a);
-    }
     return cudaGetLastError();
 }
 
@@ -417,18 +459,6 @@ int occupancy_loco_absmax(int dtype)
     if (dtype == 0) return occ_of(k_loco_absmax<float>);
     if (dtype == 1) return occ_of(k_loco_absmax<__half>);
     return occ_of(k_loco_absmax<__nv_bfloat16>);
-}
-
-int occupancy_loco_quant(int dtype, int bits)
-{
-    if (bits == 4) {
-        if (dtype == 0) return occ_of(k_loco_quant<float, 4>);
-        if (dtype == 1) return occ_of(k_loco_quant<__half, 4>);
-        return occ_of(k_loco_quant<__nv_bfloat16, 4>);
-    }
-    if (dtype == 0) return occ_of(k_loco_quant<float, 8>);
-    if (dtype == 1) return occ_of(k_loco_quant<__half, 8>);
-    return occ_of(k_loco_quant<__nv_bfloat16, 8>);
 }
 
 // The register kernel needs the chunk's group count to divide kLocoU (1, 2 or 4 groups):
@@ -474,6 +504,32 @@ int occupancy_loco_fused(int dtype, int bits, int64_t C)
     if (dtype == 1) OB_LOCO_OCC(__half, 8);
     OB_LOCO_OCC(__nv_bfloat16, 8);
 #undef OB_LOCO_OCC
+}
+
+cudaError_t launch_loco_qs(int dtype, const LocoArgs& a, int grid, cudaStream_t s)
+{
+    if (a.bits == 4) {
+        if (dtype == 0) k_loco_qs<float, 4><<<grid, kBlock, 0, s>>>(a);
+        else if (dtype == 1) k_loco_qs<__half, 4><<<grid, kBlock, 0, s>>>(a);
+        else k_loco_qs<__nv_bfloat16, 4><<<grid, kBlock, 0, s>>>(a);
+    } else {
+        if (dtype == 0) k_loco_qs<float, 8><<<grid, kBlock, 0, s>>>(a);
+        else if (dtype == 1) k_loco_qs<__half, 8><<<grid, kBlock, 0, s>>>(a);
+        else k_loco_qs<__nv_bfloat16, 8><<<grid, kBlock, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+int occupancy_loco_qs(int dtype, int bits)
+{
+    if (bits == 4) {
+        if (dtype == 0) return occ_of(k_loco_qs<float, 4>);
+        if (dtype == 1) return occ_of(k_loco_qs<__half, 4>);
+        return occ_of(k_loco_qs<__nv_bfloat16, 4>);
+    }
+    if (dtype == 0) return occ_of(k_loco_qs<float, 8>);
+    if (dtype == 1) return occ_of(k_loco_qs<__half, 8>);
+    return occ_of(k_loco_qs<__nv_bfloat16, 8>);
 }
 
 cudaError_t launch_loco_server(const LocoArgs& a, int grid, cudaStream_t s)

@@ -55,6 +55,7 @@ SIGNATURES = {
     "ob_strerror": (ctypes.c_char_p, [_int]),
     "ob_last_cuda_error": (_int, []),
     "ob_set_loco_ratio": (_int, [_vp, _f]),
+    "ob_set_loco_codes": (_int, [_vp, _int]),
     "ob_worker_compress_noalloc": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ob_noalloc_read_status": (_int, [_vp, ctypes.POINTER(ctypes.c_uint), _vp]),
 }
@@ -158,6 +159,9 @@ class Context:
 
     def set_loco_ratio(self, ratio):
         _call("ob_set_loco_ratio", self.h, float(ratio))
+
+    def set_loco_codes(self, keep):
+        _call("ob_set_loco_codes", self.h, int(bool(keep)))
 
     def set_step(self, step):
         _call("ob_set_step", self.h, step)

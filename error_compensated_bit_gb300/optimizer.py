@@ -122,7 +122,8 @@ class LocoAdam:
     """
 
     def __init__(self, n, W, chunk=None, lr=1e-4, betas=(0.9, 0.999), eps=1e-8,
-                 weight_decay=0.0, bits=4, beta=0.9, ratio=1.0, x=None, device="cuda"):
+                 weight_decay=0.0, bits=4, beta=0.9, ratio=1.0, x=None, device="cuda",
+                 keep_codes=False):
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
@@ -130,6 +131,7 @@ class LocoAdam:
             self.ctx = ob.Context(n, W, chunk or n // W, betas[0], betas[1], eps, lr)
             self.ctx.set_options(weight_decay, False)
             self.ctx.set_loco_ratio(ratio)
+            self.ctx.set_loco_codes(keep_codes)
             self.n, self.W, self.chunk = n, W, chunk or n // W
             self.bits, self.beta, self.ratio = bits, beta, ratio
             f32 = dict(dtype=torch.float32, device=self.device)
@@ -154,7 +156,9 @@ class LocoAdam:
 
     def messages(self):
         """This step's low-bit messages viewing the workspace: codes [W, n*bits/8] uint8
-        and scales [W, nchunks] float32."""
+        and scales [W, nchunks] float32. The codes are stored for chunks of up to 4096
+        elements, or when the object was made with ``keep_codes=True`` (longer chunks
+        otherwise keep them in registers)."""
         code_bytes = self.W * self.n * self.bits // 8
         off = (code_bytes + 255) // 256 * 256
         nch = self.n // self.chunk

@@ -201,8 +201,12 @@ int ob_compressed_step_host(ob_ctx *ctx, const void *grads_host, void *grads_dev
  * complement) or 8 (one signed byte). loco_err [W][n] float holds e~ (zero at start).
  * loco_ws must hold ob_loco_workspace_bytes(ctx, bits) bytes, zeroed before first use.
  * Chunks of up to 4096 elements are quantized in one pass that also finds their absmax
- * (profiled as OB_K_LOCO_QUANT; OB_K_LOCO_ABSMAX then records no launch); longer chunks
- * take a separate absmax pass first. The results are the same either way.
+ * (profiled as OB_K_LOCO_QUANT; OB_K_LOCO_ABSMAX then records no launch), and a second
+ * pass averages the codes and takes the Adam step (OB_K_LOCO_SERVER). Longer chunks take
+ * a separate absmax pass first, then one pass that quantizes every worker's row and takes
+ * the Adam step (profiled as OB_K_LOCO_QUANT; OB_K_LOCO_SERVER then records no launch);
+ * its codes never leave the registers unless ob_set_loco_codes asks for them. The
+ * results are the same either way. The scales are always stored in loco_ws.
  */
 int ob_loco_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m, float *v,
                  float *loco_err, float beta, int bits, void *loco_ws, void *stream);
@@ -214,6 +218,15 @@ int ob_loco_step(ob_ctx *ctx, const void *grads, int dtype, float *x, float *m, 
  * OB_EINVAL outside that range.
  */
 int ob_set_loco_ratio(ob_ctx *ctx, float ratio);
+
+/*
+ * Whether ob_loco_step stores the codes in loco_ws (laid out as above, at the start of
+ * the workspace) when the chunks are longer than 4096 elements: 0 (the default) keeps
+ * them in registers, saving their W*bits/8 bytes per element of DRAM writes; 1 stores
+ * them too, for inspection. Short chunks always store them. OB_EINVAL unless keep is 0
+ * or 1.
+ */
+int ob_set_loco_codes(ob_ctx *ctx, int keep);
 size_t ob_loco_workspace_bytes(const ob_ctx *ctx, int bits);
 
 /* ---- state ----------------------------------------------------------------------------- */

@@ -108,6 +108,9 @@ def test_calls_reject_bad_arguments(ob):
         assert lib.ob_set_loco_ratio(h, bad) == ob.OB_EINVAL
     for good_ratio in (0.0, 0.5, 1.0):
         assert lib.ob_set_loco_ratio(h, good_ratio) == ob.OB_OK
+    for bad_keep in (-1, 2):
+        assert lib.ob_set_loco_codes(h, bad_keep) == ob.OB_EINVAL
+    assert lib.ob_set_loco_codes(h, 1) == ob.OB_OK and lib.ob_set_loco_codes(h, 0) == ob.OB_OK
     assert lib.ob_set_step(h, -1) == ob.OB_EINVAL
     assert lib.ob_set_step(h, 41) == ob.OB_OK and lib.ob_get_step(h) == 41
     assert lib.ob_set_lr(h, float("inf")) == ob.OB_EINVAL

@@ -74,6 +74,9 @@ def test_dominant_kernel_bytes(bench):
     assert bench.dominant_kernel_bytes("compressed", n, 4, 2) == n * (4 * (2 + 8.125) + 4)
     assert bench.dominant_kernel_bytes("warmup", n, 4, 2) == n * (4 * 2 + 24)
     assert bench.dominant_kernel_bytes("loco", n, 4, 2) == n * 4 * (2 + 4 + 4 + 0.5)
+    assert bench.dominant_kernel_bytes("loco", n, 4, 2, 256) == n * 4 * (2 + 4 + 4 + 0.5)
+    # long chunks: one pass quantizes every row and takes the Adam step (x, m, v)
+    assert bench.dominant_kernel_bytes("loco", n, 4, 2, n // 4) == n * (4 * (2 + 4 + 4) + 24)
 
 
 def test_extra_workloads_cover_every_recipe(bench):

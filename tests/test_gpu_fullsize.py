@@ -100,6 +100,10 @@ def test_full_size_sampled_chunks(ora, name, W, phase, chunk):
                 assert np.array_equal(host(x, k), states[k].x), "warm-up %d chunk %d x" % (t, k)
             continue
         if phase == "loco":
+            # long chunks keep their codes in registers; the first step stores them too,
+            # to be compared, and the second runs as the benchmark does
+            keep = t == warm
+            ctx.set_loco_codes(keep)
             ctx.loco_step(g, x, m, v, ew, lws, 0.9, 4)
             outs = {k: ora.loco_step(states[k], gk[k], err[k], beta=0.9, bits=4) for k in picks}
             torch.cuda.synchronize()
@@ -109,8 +113,9 @@ def test_full_size_sampled_chunks(ora, name, W, phase, chunk):
             scales = lws[scale_off:scale_off + W * nch * 4].view(torch.float32).view(W, nch)
             for k in picks:
                 st = states[k]
-                assert np.array_equal(codes[:, k * C // 2:(k + 1) * C // 2].cpu().numpy(),
-                                      outs[k]["codes"]), "step %d chunk %d codes" % (t, k)
+                if keep or C <= 4096:
+                    assert np.array_equal(codes[:, k * C // 2:(k + 1) * C // 2].cpu().numpy(),
+                                          outs[k]["codes"]), "step %d chunk %d codes" % (t, k)
                 assert np.array_equal(scales[:, k].cpu().numpy(), outs[k]["scales"][:, 0])
                 assert_close("loco %d err" % t, ew[:, sl[k]].cpu().numpy(), err[k])
                 assert_close("loco %d x" % t, host(x, k), st.x)
