@@ -249,6 +249,7 @@ int ob_init(int64_t n, int32_t W, int64_t chunk, float b1, float b2, float eps, 
     if (c->device >= 0) {
         cudaError_t e = prepare_worker(W, c->smem_budget);
         if (e == cudaSuccess) e = prepare_server(W);
+        if (e == cudaSuccess) e = prepare_loco();
         if (e != cudaSuccess) {
             delete c;
             return cuda_fail(e);
@@ -618,9 +619,9 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     // the absmax pass, then one pass that quantizes every row and takes the server step:
     // each one resident wave, each warp a contiguous range
     if (!c->loco_occ_a[dtype]) c->loco_occ_a[dtype] = occupancy_loco_absmax(dtype);
-    if (!c->loco_occ_qs[dtype][bi]) c->loco_occ_qs[dtype][bi] = occupancy_loco_qs(dtype, bits);
+    if (!c->loco_occ_qs[dtype][bi]) c->loco_occ_qs[dtype][bi] = occupancy_loco_qs(dtype, bits, c->W);
     const int grid_a = c->sms * (c->loco_occ_a[dtype] > 0 ? c->loco_occ_a[dtype] : 2);
-    const int grid_qs = c->sms * (c->loco_occ_qs[dtype][bi] > 0 ? c->loco_occ_qs[dtype][bi] : 2);
+    const int grid_qs = c->sms * (c->loco_occ_qs[dtype][bi] > 0 ? c->loco_occ_qs[dtype][bi] : 1);
     if (int r = launch(c, OB_K_LOCO_ABSMAX, s, [&] { return launch_loco_absmax(dtype, a, grid_a, s); })) return r;
     if (int r = launch(c, OB_K_LOCO_QUANT, s, [&] { return launch_loco_qs(dtype, a, grid_qs, s); })) return r;
     c->step += 1;

@@ -148,6 +148,7 @@ WorkerConfig worker_config(int W, int dtype, int smem_budget);
 // device (a property of the kernel in that device's context).
 cudaError_t prepare_worker(int W, int smem_budget);
 cudaError_t prepare_server(int W);
+cudaError_t prepare_loco();
 cudaError_t launch_server(int W, const ServerArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_scales(const UpdateArgs& a, int grid, cudaStream_t s);
@@ -164,7 +165,7 @@ cudaError_t launch_loco_fused(int dtype, const LocoArgs& a, int grid, cudaStream
 int occupancy_server(int W);
 int occupancy_update();
 int occupancy_loco_absmax(int dtype);
-int occupancy_loco_qs(int dtype, int bits);
+int occupancy_loco_qs(int dtype, int bits, int W);
 int occupancy_loco_fused(int dtype, int bits, int64_t C);
 
 // Launch `kernel` with the programmatic stream-serialization attribute (see pdl_wait in

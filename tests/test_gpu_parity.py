@@ -297,13 +297,16 @@ def test_warmup_then_compressed(ora):
     (4, "bf16", 4, 2, 1.0, False), (2, "f32", 8, 2, 1.0, True), (3, "f16", 4, 2, 1.0, False),
     (4, "bf16", 4, 400, 1.0, False), (2, "f32", 8, 25, 1.0, True),
     (4, "bf16", 4, 2, 0.5, True), (3, "f16", 8, 25, 0.0, False), (2, "f32", 4, 400, 0.3, True),
-    (2, "bf16", 4, 200, 1.0, False), (3, "f32", 8, 100, 0.5, False), (2, "f16", 4, 400 // 3, 1.0, True)])
+    (2, "bf16", 4, 200, 1.0, False), (3, "f32", 8, 100, 0.5, False), (2, "f16", 4, 400 // 3, 1.0, True),
+    (2, "bf16", 8, 2, 0.5, True), (6, "f16", 4, 2, 1.0, True)])
 def test_loco_parity(ora, W, dtype, bits, per_row, ratio, keep):
     """per_row chunks per worker row: 400, 200 and 100 make chunks of one, two and four
     256-element groups (quantized in one pass from registers), 133 chunks of three groups
     and 25 chunks of 4096 elements (one pass, read twice through the L2), 2 long chunks
     (separate absmax pass, then one pass that quantizes every row and takes the Adam step,
-    its codes in registers unless `keep` asks for them; short chunks store them anyway).
+    its codes in registers unless `keep` asks for them; short chunks store them anyway;
+    16-bit gradients with W <= 4 stage each lane's rows in shared memory, the others
+    keep them in registers).
     ratio: the share of the averaged error compensated into the gradient (1 is plain
     c = g + e~)."""
     from error_compensated_bit_gb300 import ob
