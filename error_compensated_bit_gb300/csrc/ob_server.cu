@@ -315,12 +315,15 @@ __global__ void __launch_bounds__(kBlock) k_update(UpdateArgs a)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t gi = gb + u;
-            uint32_t sbu = sb[u], mbu = 0xffu;
+            uint32_t sbu, mbu;
             if (masked) {
                 // this lane's 8 bits of group gi: byte (lane & 3) of the group's word lane >> 2
                 const int src = u * 8 + (lane >> 2);
                 sbu = (__shfl_sync(kFull, swd, src) >> (8 * (lane & 3))) & 0xffu;
                 mbu = (__shfl_sync(kFull, mwd, src) >> (8 * (lane & 3))) & 0xffu;
+            } else {
+                sbu = sb[u];
+                mbu = 0xffu;
             }
             if (gi < g_end) {
                 const int64_t e0 = gi * 256 + lane * 8;
