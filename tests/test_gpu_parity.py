@@ -298,7 +298,7 @@ def test_warmup_then_compressed(ora):
     (4, "bf16", 4, 400, 1.0, False), (2, "f32", 8, 25, 1.0, True),
     (4, "bf16", 4, 2, 0.5, True), (3, "f16", 8, 25, 0.0, False), (2, "f32", 4, 400, 0.3, True),
     (2, "bf16", 4, 200, 1.0, False), (3, "f32", 8, 100, 0.5, False), (2, "f16", 4, 400 // 3, 1.0, True),
-    (2, "bf16", 8, 2, 0.5, True), (6, "f16", 4, 2, 1.0, True)])
+    (2, "bf16", 8, 2, 0.5, True), (6, "f16", 4, 2, 1.0, True), (1, "bf16", 4, 2, 1.0, True)])
 def test_loco_parity(ora, W, dtype, bits, per_row, ratio, keep):
     """per_row chunks per worker row: 400, 200 and 100 make chunks of one, two and four
     256-element groups (quantized in one pass from registers), 133 chunks of three groups
