@@ -616,8 +616,9 @@ int ob_loco_step(ob_ctx* c, const void* grads, int dtype, float* x, float* m, fl
     }
     const cudaError_t e = cudaMemsetAsync(a.amax_bits, 0, (size_t)c->W * c->nchunks * 4, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    // the absmax pass, then one pass that quantizes every row and takes the server step:
-    // each one resident wave, each warp a contiguous range
+    // the absmax pass (a contiguous range per warp), then one pass that quantizes every row
+    // and takes the server step (a contiguous range per block, its warps taking the groups
+    // in turn): each one resident wave
     if (!c->loco_occ_a[dtype]) c->loco_occ_a[dtype] = occupancy_loco_absmax(dtype);
     if (!c->loco_occ_qs[dtype][bi]) c->loco_occ_qs[dtype][bi] = occupancy_loco_qs(dtype, bits, c->W);
     const int grid_a = c->sms * (c->loco_occ_a[dtype] > 0 ? c->loco_occ_a[dtype] : 2);
